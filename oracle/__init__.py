@@ -1,0 +1,210 @@
+"""CPU oracle for the MoE finalize + residual + RMSNorm path.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only users.  The product package never
+imports this module, and this module never imports the product package.
+
+The arithmetic lives in ``mfr_oracle.c`` (plain C, one token and one column at
+a time); this file only builds/loads it and marshals NumPy arrays.  BF16 data
+crosses as ``uint16`` bit patterns.
+
+Pins: every function here is checked in ``tests/test_oracle.py`` against
+values fixed by the pages or by mathematics (a hand-worked example, closed
+forms, brute force with exact rationals, a library BF16 rounding, a library
+RMSNorm, invariants); ``tests/test_oracle_mutations.py`` shows that planted
+mistakes in the C source fail those pins.  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "mfr_oracle.c")
+LIBRARY = os.path.join(_HERE, "libmfr_oracle.so")
+
+CFLAGS = ["-O2", "-std=c11", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
+def compile_oracle(src: str, out: str) -> str:
+    """gcc with no FMA contraction and no fast-math, so FMAs are only where
+    the source writes fmaf()."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(LIBRARY) or \
+            os.path.getmtime(LIBRARY) < os.path.getmtime(SOURCE):
+        compile_oracle(SOURCE, LIBRARY)
+    return LIBRARY
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return np.ascontiguousarray(a)
+
+
+def bf16_bits_to_f64(b) -> np.ndarray:
+    """Exact widening of BF16 bit patterns (uint16) to double (NumPy only)."""
+    b = np.asarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+class Oracle:
+    """ctypes front end of one compiled copy of the oracle."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        lib.mfr_oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.mfr_oracle_bf16_to_f64.restype = ctypes.c_double
+        lib.mfr_oracle_bf16_from_f64.argtypes = [ctypes.c_double]
+        lib.mfr_oracle_bf16_from_f64.restype = ctypes.c_uint16
+        lib.mfr_oracle_bf16_from_f64_array.argtypes = [p, p, i64]
+        lib.mfr_oracle_bf16_from_f64_array.restype = None
+        lib.mfr_oracle_weighted_residual.argtypes = [i64, i64, i64, i64, p, p, p, p, p, p, i64]
+        lib.mfr_oracle_weighted_residual.restype = i64
+        lib.mfr_oracle_rmsnorm_f64.argtypes = [i64, i64, p, p, ctypes.c_float, p]
+        lib.mfr_oracle_rmsnorm_f64.restype = None
+        lib.mfr_oracle_finalize_residual_rmsnorm.argtypes = [
+            i64, i64, i64, i64, p, p, p, p, p, ctypes.c_float, p, p, p, i64, p]
+        lib.mfr_oracle_finalize_residual_rmsnorm.restype = i64
+        lib.mfr_oracle_finalize_only.argtypes = [i64, i64, i64, i64, p, p, p, p, p, i64]
+        lib.mfr_oracle_finalize_only.restype = i64
+        self.lib = lib
+        self.path = path
+
+    # -- BF16 -----------------------------------------------------------------
+    def bf16_from_f64(self, x) -> np.ndarray:
+        """Nearest BF16 (ties to even) of each double, one rounding; uint16."""
+        x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.lib.mfr_oracle_bf16_from_f64_array(_ptr(x), _ptr(out), x.size)
+        return out
+
+    def bf16_to_f64(self, b) -> np.ndarray:
+        b = np.asarray(b, dtype=np.uint16)
+        f = np.vectorize(self.lib.mfr_oracle_bf16_to_f64, otypes=[np.float64])
+        return f(b) if b.size else b.astype(np.float64)
+
+    # -- the path, step by step ----------------------------------------------
+    @staticmethod
+    def _tokens(tokens, T):
+        if tokens is None:
+            return None, T
+        tk = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64).reshape(-1))
+        if tk.size and (tk.min() < 0 or tk.max() >= T):
+            raise IndexError("token index out of range")
+        return tk, tk.size
+
+    def weighted_residual(self, expert_out_bits, permuted_row_of, topk_weights,
+                          residual_in, tokens: Optional[Sequence[int]] = None):
+        """x = residual_in + sum_j w[t,j] * E[idx[t,j]], FP32 FMAs in slot
+        order.  Returns (x float32 [n, H], number of out-of-range slots)."""
+        E = _c(expert_out_bits, np.uint16)
+        idx = _c(permuted_row_of, np.int32)
+        w = _c(topk_weights, np.float32)
+        res = _c(residual_in, np.float32)
+        R, H = E.shape
+        T, k = idx.shape
+        assert w.shape == (T, k) and res.shape == (T, H)
+        tk, n = self._tokens(tokens, T)
+        x = np.empty((n, H), dtype=np.float32)
+        bad = self.lib.mfr_oracle_weighted_residual(T, H, k, R, _ptr(E), _ptr(idx), _ptr(w),
+                                                    _ptr(res), _ptr(x), _ptr(tk), n)
+        return x, int(bad)
+
+    def rmsnorm_f64(self, x, gamma_bits, eps: float) -> np.ndarray:
+        """y = x / sqrt(mean(x^2) + eps) * gamma, in double, row by row."""
+        x = _c(x, np.float32)
+        g = _c(gamma_bits, np.uint16)
+        n, H = x.shape
+        assert g.shape == (H,)
+        y = np.empty((n, H), dtype=np.float64)
+        self.lib.mfr_oracle_rmsnorm_f64(n, H, _ptr(x), _ptr(g), ctypes.c_float(eps), _ptr(y))
+        return y
+
+    def finalize_residual_rmsnorm(self, expert_out_bits, permuted_row_of, topk_weights,
+                                  residual_in, gamma_bits, eps: float,
+                                  tokens: Optional[Sequence[int]] = None):
+        """The whole path for the given tokens (all when None).
+
+        Returns (residual_out float32 [n, H], out uint16 [n, H] BF16 bits,
+        number of out-of-range slots)."""
+        E = _c(expert_out_bits, np.uint16)
+        idx = _c(permuted_row_of, np.int32)
+        w = _c(topk_weights, np.float32)
+        res = _c(residual_in, np.float32)
+        g = _c(gamma_bits, np.uint16)
+        R, H = E.shape
+        T, k = idx.shape
+        assert w.shape == (T, k) and res.shape == (T, H) and g.shape == (H,)
+        tk, n = self._tokens(tokens, T)
+        res_out = np.empty((n, H), dtype=np.float32)
+        out = np.empty((n, H), dtype=np.uint16)
+        scratch = np.empty(H, dtype=np.float64)
+        bad = self.lib.mfr_oracle_finalize_residual_rmsnorm(
+            T, H, k, R, _ptr(E), _ptr(idx), _ptr(w), _ptr(res), _ptr(g), ctypes.c_float(eps),
+            _ptr(res_out), _ptr(out), _ptr(tk), n, _ptr(scratch))
+        return res_out, out, int(bad)
+
+    def finalize_only(self, expert_out_bits, permuted_row_of, topk_weights,
+                      tokens: Optional[Sequence[int]] = None):
+        """out = BF16(sum_j w[t,j] * E[idx[t,j]]), the FP32 FMA sum rounded
+        once.  Returns (out uint16 [n, H], number of out-of-range slots)."""
+        E = _c(expert_out_bits, np.uint16)
+        idx = _c(permuted_row_of, np.int32)
+        w = _c(topk_weights, np.float32)
+        R, H = E.shape
+        T, k = idx.shape
+        tk, n = self._tokens(tokens, T)
+        out = np.empty((n, H), dtype=np.uint16)
+        bad = self.lib.mfr_oracle_finalize_only(T, H, k, R, _ptr(E), _ptr(idx), _ptr(w),
+                                                _ptr(out), _ptr(tk), n)
+        return out, int(bad)
+
+
+_default: Optional[Oracle] = None
+_lock = threading.Lock()
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def bf16_from_f64(x):
+    return default().bf16_from_f64(x)
+
+
+def weighted_residual(*a, **kw):
+    return default().weighted_residual(*a, **kw)
+
+
+def rmsnorm_f64(*a, **kw):
+    return default().rmsnorm_f64(*a, **kw)
+
+
+def finalize_residual_rmsnorm(*a, **kw):
+    return default().finalize_residual_rmsnorm(*a, **kw)
+
+
+def finalize_only(*a, **kw):
+    return default().finalize_only(*a, **kw)

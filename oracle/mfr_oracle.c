@@ -1,0 +1,230 @@
+/*
+ * CPU oracle for the MoE finalize + residual + RMSNorm path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link,
+ * load or call this file: only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library.
+ *
+ * It is deliberately plain and slow: one token at a time, one column at a
+ * time, no blocking, no vectors, no threads.  Build with
+ *     gcc -O2 -std=c11 -fno-fast-math -ffp-contract=off -fPIC -shared -lm
+ * so that a fused multiply-add happens only where fmaf() is written.
+ *
+ * What it computes, and where each step is stated:
+ *
+ *  [A] "FlashInfer MoE 성능 최적화: CuTe DSL을 활용한 Deterministic Finalize
+ *      개선기" (flashinfer PR 5319 analysis), section 1, the new CuTe-DSL
+ *      finalize kernel: the k expert outputs of a token are accumulated with
+ *      FP32 fused multiply-adds (round to nearest) and converted to BF16 only
+ *      at the very end; the unfused finalize is the deterministic one.
+ *  [B] "Blackwell 아키텍처를 위한 MoE All-Reduce Fusion 최적화: FlashInfer의
+ *      'Cake' 백엔드 분석" (flashinfer PR 4730 analysis), section 2, the fusion
+ *      strategy: sum the expert outputs, add the residual, then RMSNorm, all
+ *      in one pass.
+ *  [C] "FlashInfer, Muse-Spark-Open을 위한 융합 정규화 및 TP/EP MoE 최적화로
+ *      성능 극대화" (flashinfer PR 6544 analysis), section 1.1 (the residual
+ *      stream is kept in FP32) and section 2.1 (the finalize reads the rows
+ *      straight from the GEMM2 result, i.e. in expert-grouped order through
+ *      an index map).
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes): the accumulator starts at +0 and the residual is added once after
+ * the k slots; slots run j = 0..k-1 in the order stored; weights are used as
+ * given; FMA without flush-to-zero; RMS over the FP32 updated residual with
+ * eps inside the square root; y = x / rms * gamma (not 1 + gamma); an index
+ * outside [0, R) makes its slot contribute nothing and is counted.
+ *
+ * Precision: steps [A] and the residual add are FP32, exactly as the pages fix
+ * them.  The normalisation is not fixed by the pages, so the oracle computes
+ * it in double and rounds once, from double, to BF16 (nearest, ties to even).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+/* ---- BF16 <-> binary64 ---------------------------------------------------- */
+
+/* A BF16 value is the upper half of the FP32 encoding; widening is exact. */
+double mfr_oracle_bf16_to_f64(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static float bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * Nearest BF16 to a double, ties to even, with a single rounding.
+ * BF16 has 8 significant bits, exponents -126..127 for normal numbers and a
+ * fixed spacing of 2^-133 below 2^-126.  The value is divided by its BF16
+ * spacing (a power of two, so exactly), rounded to an integer with the
+ * default nearest-even mode, and multiplied back.  Results at or above 2^128
+ * overflow to infinity.  NaN maps to the quiet NaN 0x7FC0 with its sign.
+ */
+uint16_t mfr_oracle_bf16_from_f64(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(x);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);          /* a in [2^(e-1), 2^e) */
+    int lead = e - 1;            /* exponent of the leading bit */
+    if (lead < -126)
+        lead = -126;             /* subnormal range: fixed spacing */
+    double spacing = ldexp(1.0, lead - 7);
+    double q = nearbyint(a / spacing);
+    double r = q * spacing;
+    if (r >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80u);
+    float f = (float)r;          /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFFu));
+}
+
+void mfr_oracle_bf16_from_f64_array(const double* x, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = mfr_oracle_bf16_from_f64(x[i]);
+}
+
+/* ---- steps a3-a5: gather, FP32 weighted sum, residual --------------------- */
+
+static int slot_valid(int32_t r, int64_t R)
+{
+    return r >= 0 && (int64_t)r < R;
+}
+
+/* Number of slots of token t whose index lies outside [0, R). */
+static int64_t count_bad_slots(int64_t t, int64_t k, int64_t R, const int32_t* idx)
+{
+    int64_t bad = 0;
+    for (int64_t j = 0; j < k; ++j)
+        if (!slot_valid(idx[t * k + j], R))
+            ++bad;
+    return bad;
+}
+
+/*
+ * acc = +0; for j = 0..k-1: acc = fmaf(w[t,j], E[idx[t,j], h], acc)   [A]
+ * x   = residual_in[t, h] + acc   (one FP32 add)                       [B][C]
+ * Rows i of x correspond to tokens[i] (or to i when tokens is NULL).
+ * Returns the number of (token, slot) pairs whose index was out of range.
+ */
+int64_t mfr_oracle_weighted_residual(int64_t T, int64_t H, int64_t k, int64_t R,
+                                     const uint16_t* expert_out, const int32_t* idx,
+                                     const float* w, const float* residual_in,
+                                     float* x, const int64_t* tokens, int64_t ntokens)
+{
+    int64_t bad = 0;
+    int64_t n = tokens ? ntokens : T;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        bad += count_bad_slots(t, k, R, idx);
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int64_t j = 0; j < k; ++j) {
+                int32_t r = idx[t * k + j];
+                if (!slot_valid(r, R))
+                    continue;
+                float e = bf16_to_f32(expert_out[(int64_t)r * H + h]);
+                acc = fmaf(w[t * k + j], e, acc);
+            }
+            x[i * H + h] = residual_in[t * H + h] + acc;
+        }
+    }
+    return bad;
+}
+
+/* ---- steps a6-a7: RMSNorm in double --------------------------------------- */
+
+/*
+ * y[h] = x[h] / sqrt(mean_h(x^2) + eps) * gamma[h], in double, for n rows of
+ * width H.  This is the plain definition of RMSNorm applied to the updated
+ * FP32 residual [B].
+ */
+void mfr_oracle_rmsnorm_f64(int64_t n, int64_t H, const float* x,
+                            const uint16_t* gamma, float eps, double* y)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const float* xr = x + i * H;
+        double ss = 0.0;
+        for (int64_t h = 0; h < H; ++h)
+            ss += (double)xr[h] * (double)xr[h];
+        double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
+        for (int64_t h = 0; h < H; ++h)
+            y[i * H + h] = (double)xr[h] * inv * mfr_oracle_bf16_to_f64(gamma[h]);
+    }
+}
+
+/* ---- the whole path ------------------------------------------------------- */
+
+/*
+ * residual_out[i, :] = x of token tokens[i] (FP32);
+ * out[i, :]          = BF16(RMSNorm(x) * gamma), one rounding from double.
+ * Works one token at a time so a sampled subset of a large workload needs
+ * only H doubles of scratch, which the caller passes in ``y_scratch``.
+ */
+int64_t mfr_oracle_finalize_residual_rmsnorm(
+    int64_t T, int64_t H, int64_t k, int64_t R,
+    const uint16_t* expert_out, const int32_t* idx, const float* w,
+    const float* residual_in, const uint16_t* gamma, float eps,
+    float* residual_out, uint16_t* out,
+    const int64_t* tokens, int64_t ntokens, double* y_scratch)
+{
+    int64_t bad = 0;
+    int64_t n = tokens ? ntokens : T;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        float* xr = residual_out + i * H;
+        bad += mfr_oracle_weighted_residual(T, H, k, R, expert_out, idx, w,
+                                            residual_in, xr, &t, 1);
+        mfr_oracle_rmsnorm_f64(1, H, xr, gamma, eps, y_scratch);
+        for (int64_t h = 0; h < H; ++h)
+            out[i * H + h] = mfr_oracle_bf16_from_f64(y_scratch[h]);
+    }
+    return bad;
+}
+
+/*
+ * Finalize only (no residual, no norm): out = BF16(acc) with acc the FP32
+ * weighted sum of [A].  This is the plain "MoE finalize" of the PR 5319 page.
+ */
+int64_t mfr_oracle_finalize_only(int64_t T, int64_t H, int64_t k, int64_t R,
+                                 const uint16_t* expert_out, const int32_t* idx,
+                                 const float* w, uint16_t* out,
+                                 const int64_t* tokens, int64_t ntokens)
+{
+    int64_t bad = 0;
+    int64_t n = tokens ? ntokens : T;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        bad += count_bad_slots(t, k, R, idx);
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int64_t j = 0; j < k; ++j) {
+                int32_t r = idx[t * k + j];
+                if (!slot_valid(r, R))
+                    continue;
+                acc = fmaf(w[t * k + j], bf16_to_f32(expert_out[(int64_t)r * H + h]), acc);
+            }
+            out[i * H + h] = mfr_oracle_bf16_from_f64((double)acc);
+        }
+    }
+    return bad;
+}
