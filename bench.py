@@ -1,0 +1,466 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused MoE finalize + residual + RMSNorm path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill]
+                    [--impl ours|reference] [--sweep] [--no-cpu-baseline]
+
+One step = one call of the whole path (gather, FP32 weighted sum, residual
+update, RMSNorm, bf16 store) over one batch of synthetic inputs already
+resident in HBM.  The headline workload is the prefill configuration
+(T=16384 tokens, H=4096, top-8, 128 experts, Zipf(1.2) routing); its inputs
+(1.75 GB per call) are far larger than L2, and two input/output sets are
+alternated so no step starts with its data in L2.
+
+The metric is effective HBM bandwidth: algorithmic bytes per call
+(T*k*H*2 + T*H*(4+4+2) + T*k*8) divided by the device time of a call.
+
+Under torchrun each rank runs its own independent batch on its own GPU
+(tokens are independent, so the path shards with no collective): weak
+scaling, value = all ranks' bytes / the slowest rank's time.
+
+--impl reference times the CPU oracle (the plain C reference) on the host
+cores on a bounded sample of the same workload, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "effective HBM GB/s (% of GB300 peak) and µs/call vs tokens T, H=4096/8192, k=8"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["moe_finalize_residual_rmsnorm_gb300/csrc/mfr_rows.cu",
+                  "moe_finalize_residual_rmsnorm_gb300/csrc/mfr_device.cuh"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="prefill", choices=sorted(W.all_named()))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sweep", action="store_true", help="also time the decode and wide sweeps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--no-pdl", action="store_true")
+    return ap.parse_args(argv)
+
+
+# --- distributed plumbing ---------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# --- clocks -----------------------------------------------------------------------
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        loaded = [v for v in sm if smax and v > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --- helpers ------------------------------------------------------------------------
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, variant: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload, {})
+    if e.get("kernel_hash") != kernel_source_hash() or e.get("variant") != variant:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --- CPU oracle timing ------------------------------------------------------------------
+
+def time_oracle(inp_host: dict, n_tokens: int, threads: int, rng_seed: int = 0):
+    """Runs the oracle on n_tokens sampled tokens split over `threads` host
+    threads (the C calls release the GIL).  Returns (seconds, tokens)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    T = inp_host["idx"].shape[0]
+    rng = np.random.default_rng(rng_seed)
+    tokens = np.sort(rng.choice(T, size=min(n_tokens, T), replace=False))
+    parts = [p for p in np.array_split(tokens, threads) if p.size]
+    orc = oracle.default()
+
+    def work(tk):
+        return orc.finalize_residual_rmsnorm(inp_host["E"], inp_host["idx"], inp_host["w"], inp_host["res"],
+                                             inp_host["gamma"], inp_host["eps"], tokens=tk)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        list(ex.map(work, parts))
+    return time.perf_counter() - t0, int(tokens.size)
+
+
+def host_copy(inp):
+    def bits16(t):
+        return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return {"E": bits16(inp["expert_out"]), "idx": inp["permuted_row_of"].cpu().numpy(),
+            "w": inp["topk_weights"].cpu().numpy(), "res": inp["residual"].cpu().numpy(),
+            "gamma": bits16(inp["gamma"]), "eps": inp["eps"]}
+
+
+def calibrate_tokens(inp_host, T: int, target_s: float, cores: int) -> int:
+    """Number of sampled tokens the oracle processes in about target_s."""
+    n = min(T, cores * 4)
+    while True:
+        dt, n = time_oracle(inp_host, n, cores, 1)
+        if n >= T or dt >= 0.5 * target_s:
+            break
+        n = int(min(T, n * min(16.0, max(2.0, 0.9 * target_s / max(dt, 1e-6)))))
+    return int(min(T, max(cores, n * target_s / max(dt, 1e-6))))
+
+
+def cpu_baseline(inp_host, wl, target_s: float):
+    cores = host_cores()
+    n_tokens = calibrate_tokens(inp_host, wl.T, target_s, cores)
+    dt, n = time_oracle(inp_host, n_tokens, cores, 2)
+    gbs = W.algorithmic_bytes(n, wl.H, wl.k) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {wl.T} tokens (seeded sample), H={wl.H}, k={wl.k}, {dt:.2f} s wall, "
+                      f"{cores} host threads"}
+
+
+# --- the GPU arm -------------------------------------------------------------------------
+
+def run_ours(args):
+    import moe_finalize_residual_rmsnorm_gb300 as mfr
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    wl = W.by_name(args.workload).with_(seed=W.by_name(args.workload).seed + rank)
+    T, H, k, R = wl.T, wl.H, wl.k, wl.R
+    nbytes = W.algorithmic_bytes(T, H, k)
+
+    mfr.load_library()
+    plan = mfr.Plan(T, H, k, R, enable_pdl=not args.no_pdl)
+    info = plan.info()
+
+    # two independent input/output sets, alternated every step
+    sets = []
+    for s in range(2):
+        inp = W.make_inputs(wl.with_(seed=wl.seed * 2 + s), device)
+        inp["residual_out"] = torch.empty_like(inp["residual"])
+        inp["out"] = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        sets.append(inp)
+    stream = torch.cuda.Stream(device)
+
+    def step(i):
+        d = sets[i & 1]
+        plan.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["residual"], d["residual_out"],
+                 d["gamma"], d["eps"], d["out"], stream, validate=False)
+
+    torch.cuda.synchronize(device)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(dist, device)
+        torch.cuda.synchronize(device)
+        start.record(stream)
+        for i in range(args.steps):
+            step(i)
+        stop.record(stream)
+        stop.synchronize()
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+    ms_local = start.elapsed_time(stop) / args.steps
+    ms = max_over_ranks(dist, ms_local, device)
+    if plan.get_status(stream) != 0:
+        raise RuntimeError("the device status word reported an out-of-range index")
+
+    value = nbytes * world / (ms * 1e-3) / 1e9
+    achieved = nbytes / (ms_local * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic = recorded_traffic(args.workload, info["variant_name"])
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, plan, sets[0], nbytes, world, dist, device)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "us_per_call": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32 accumulate, bf16 out", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: T={T} H={H} k={k} E={wl.E} routing={wl.routing}"
+                               f"{'(s=%g)' % wl.zipf_s if wl.routing == 'zipf' else ''}",
+                   "tokens_per_gpu": T, "hidden": H, "top_k": k, "experts": wl.E,
+                   "bytes_per_call": nbytes, "variant": info["variant_name"], "grid": info["grid_x"],
+                   "block": info["block"], "cluster": info["cluster"], "pdl": not args.no_pdl,
+                   "l2": "inputs larger than L2 (1.75 GB/call) and 2 alternating input sets",
+                   "parallelism": f"replicas x{world} (independent token batches)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": traffic, "algorithmic_bytes": nbytes,
+                     "kernel": "rows_kernel" if info["variant_name"] != "cluster" else "rows_kernel(cluster)"},
+        "clocks": clocks.summary(),
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+    }
+    if args.sweep:
+        result["sweep"] = run_sweep(mfr, device, args)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(host_copy(sets[0]), wl, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, plan, dev, nbytes, world, dist, device):
+    import moe_finalize_residual_rmsnorm_gb300 as mfr
+    host_in = {key: dev[key].cpu().pin_memory() for key in
+               ("expert_out", "permuted_row_of", "topk_weights", "residual", "gamma")}
+    host_in["eps"] = dev["eps"]
+    host_out = {"residual_out": torch.empty(dev["residual_out"].shape, dtype=torch.float32).pin_memory(),
+                "out": torch.empty(dev["out"].shape, dtype=torch.bfloat16).pin_memory()}
+    stream = torch.cuda.Stream(device)
+    steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        mfr.finalize_residual_rmsnorm_host(plan, host_in, dev, host_out, stream)
+    stream.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    start.record(stream)
+    h2d = d2h = 0
+    for _ in range(steps):
+        h2d, d2h = mfr.finalize_residual_rmsnorm_host(plan, host_in, dev, host_out, stream)
+    stop.record(stream)
+    stop.synchronize()
+    ms = max_over_ranks(dist, start.elapsed_time(stop) / steps, device)
+    return {"value": round(nbytes * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4),
+            "steps": steps}
+
+
+def run_sweep(mfr, device, args):
+    """µs/call and GB/s at each decode and wide size (auto plan, L2 defeated
+    by rotating buffer sets whose total exceeds 3x L2)."""
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    rows = []
+    for wl in [W.decode(t) for t in W.DECODE_TOKENS] + [W.wide(t) for t in W.WIDE_TOKENS]:
+        nbytes = W.algorithmic_bytes(wl.T, wl.H, wl.k)
+        nsets = int(min(64, max(2, -(-3 * l2 // max(nbytes, 1)))))
+        base = W.make_inputs(wl, device)
+        sets = []
+        for s in range(nsets):
+            d = {key: (v.clone() if isinstance(v, torch.Tensor) else v) for key, v in base.items()}
+            d["residual_out"] = torch.empty_like(d["residual"])
+            d["out"] = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device)
+            sets.append(d)
+        plan = mfr.Plan(wl.T, wl.H, wl.k, wl.R, enable_pdl=not args.no_pdl)
+        stream = torch.cuda.Stream(device)
+        n = 200 if wl.T <= 512 else 40
+
+        def go(i):
+            d = sets[i % nsets]
+            plan.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["residual"],
+                     d["residual_out"], d["gamma"], d["eps"], d["out"], stream, validate=False)
+        for i in range(10):
+            go(i)
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(n):
+            go(i)
+        b.record(stream)
+        b.synchronize()
+        us = a.elapsed_time(b) / n * 1e3
+        info = plan.info()
+        rows.append({"workload": wl.name, "T": wl.T, "H": wl.H, "us_per_call": round(us, 3),
+                     "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1), "variant": info["variant_name"],
+                     "cluster": info["cluster"], "sets": nsets})
+        del sets, base
+    return rows
+
+
+# --- the reference arm: the CPU oracle ------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl = W.by_name(args.workload)
+    inp = W.make_inputs(wl, "cpu")
+    host = host_copy(inp)
+    cores = host_cores()
+    total_budget = 150.0
+    per_step = max(0.5, min(args.cpu_seconds, total_budget / max(1, args.steps + args.warmup)))
+    n_tokens = calibrate_tokens(host, wl.T, per_step, cores)
+    for i in range(args.warmup):
+        time_oracle(host, n_tokens, cores, 100 + i)
+    times = []
+    for i in range(args.steps):
+        dt, n = time_oracle(host, n_tokens, cores, 1000 + i)
+        times.append(dt)
+    s = sum(times) / len(times)
+    gbs = W.algorithmic_bytes(n_tokens, wl.H, wl.k) / s / 1e9
+    sample = (f"{n_tokens} of {wl.T} tokens per step (seeded samples), H={wl.H}, k={wl.k}, "
+              f"{s:.2f} s per step, {cores} host threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 accumulate, bf16 out", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: T={wl.T} H={wl.H} k={wl.k} E={wl.E}", "tokens_per_gpu": wl.T},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        print("bench.py: --warmup must be >= 3", file=sys.stderr)
+        return 2
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        if not torch.cuda.is_available():
+            print("bench.py: no CUDA device", file=sys.stderr)
+            return 1
+        run_ours(args)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+/*
+ * moe_finalize_rmsnorm.h — C ABI of the GB300 (sm_103a) MoE finalize +
+ * residual + RMSNorm library (libmfr.so).
+ *
+ * The operation, for every token t in [0, T) and column h in [0, H):
+ *
+ *   acc          = +0;  for j = 0..k-1:  acc = fma(w[t,j], E[idx[t,j], h], acc)
+ *   x            = residual_in[t,h] + acc                          (FP32)
+ *   residual_out[t,h] = x
+ *   out[t,h]     = bf16( x / sqrt(mean_h(x^2) + eps) * gamma[h] )
+ *
+ * Where each step is defined:
+ *  - Gather of the k expert rows straight from the GEMM2 result, which sits in
+ *    expert-grouped order and is reached through the index map
+ *    permuted_row_of: "FlashInfer, Muse-Spark-Open을 위한 융합 정규화 및 TP/EP
+ *    MoE 최적화로 성능 극대화" (flashinfer PR 6544 analysis), section 2.1.
+ *  - Weighted sum with FP32 fused multiply-adds, in a fixed slot order, BF16
+ *    only at the end; the unfused finalize is the deterministic one:
+ *    "FlashInfer MoE 성능 최적화: CuTe DSL을 활용한 Deterministic Finalize
+ *    개선기" (flashinfer PR 5319 analysis), section 1.
+ *  - Residual add on the FP32 residual stream, then RMSNorm, in one pass:
+ *    "Blackwell 아키텍처를 위한 MoE All-Reduce Fusion 최적화: FlashInfer의
+ *    'Cake' 백엔드 분석" (flashinfer PR 4730 analysis), section 2 (fusion
+ *    strategy); FP32 residual stream: PR 6544 analysis, section 1.1.
+ *  - Programmatic dependent launch: the kernel loads its independent inputs,
+ *    then waits for the producing kernel before touching its output:
+ *    PR 5319 analysis, section 2.
+ *  - A thread-block cluster that reduces through distributed shared memory
+ *    for few tokens: PR 4730 analysis, section 2 (cluster-level exchange).
+ *  The all-reduce across GPUs that those pages fuse in is not part of this
+ *  single-GPU library.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device (or managed) addresses on the
+ *    plan's device; the caller owns all of them.  No entry point allocates on
+ *    a run: only moe_finalize_rmsnorm_plan allocates (a 4-byte device status
+ *    word), and moe_finalize_rmsnorm_destroy frees it.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Runs are asynchronous on that stream.
+ *  - Every function returns MFR_OK or an MFR_ERR_* code and never aborts the
+ *    process.  moe_finalize_rmsnorm_last_error() gives a one-line reason for
+ *    the last failure on the calling thread.
+ *  - Layouts are dense row-major: expert_out [R, H] bf16, permuted_row_of
+ *    [T, k] int32, topk_weights [T, k] fp32, residual_in / residual_out
+ *    [T, H] fp32, gamma [H] bf16, out [T, H] bf16.
+ */
+#ifndef MOE_FINALIZE_RMSNORM_H
+#define MOE_FINALIZE_RMSNORM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------- */
+#define MFR_OK                    0
+#define MFR_ERR_INVALID_ARG       1  /* null pointer, eps < 0 or not finite, bad alias, wrong device */
+#define MFR_ERR_UNSUPPORTED_SHAPE 2  /* see moe_finalize_rmsnorm_supports */
+#define MFR_ERR_MISALIGNED        3  /* 16-byte rule for E/residual/gamma/out, 4-byte for idx/w */
+#define MFR_ERR_BAD_DEVICE        4  /* the current device is not compute capability 10.3 */
+#define MFR_ERR_LAUNCH            5  /* the kernel launch failed (CUDA error wrapped) */
+#define MFR_ERR_CUDA              6  /* another CUDA runtime call failed */
+#define MFR_ERR_BAD_INDEX         7  /* a permuted_row_of entry was outside [0, R) */
+
+/* ---- bits of the device status word ------------------------------------- */
+#define MFR_STATUS_BAD_INDEX      1  /* some slot index was outside [0, R); that slot added 0 */
+
+/* ---- kernel variants ---------------------------------------------------- */
+#define MFR_VARIANT_AUTO          0  /* chosen from (T, H, k, device) only  */
+#define MFR_VARIANT_CLUSTER       1  /* H split over a cluster of CTAs per token, DSMEM reduction */
+#define MFR_VARIANT_ROWS          2  /* one CTA per token, rows gathered into registers */
+#define MFR_VARIANT_STREAM        3  /* persistent CTAs, rows staged in shared memory by bulk copies */
+
+/* Options of a plan.  Zero-initialise, or call moe_finalize_rmsnorm_default_options. */
+typedef struct mfr_options {
+    int enable_pdl;    /* 1: launch with programmatic stream serialization; the kernel
+                          reads permuted_row_of, topk_weights and gamma BEFORE waiting
+                          on the preceding kernel in the stream, and expert_out and
+                          residual_in after.  Those three must therefore not be written
+                          by a kernel that may still be running when this one starts.
+                          0: ordinary stream order. */
+    int force_variant; /* MFR_VARIANT_*; AUTO picks by T, H and the device */
+    int cluster_size;  /* MFR_VARIANT_CLUSTER: CTAs per token (2, 4, 8 or 16); 0 = auto */
+    int debug_checks;  /* 1: run() waits for the kernel and returns MFR_ERR_BAD_INDEX
+                          when a slot index was out of range (slow; for debugging) */
+} mfr_options;
+
+/* What a plan decided; for tests, benchmarks and logs. */
+typedef struct mfr_plan_info {
+    int variant;       /* MFR_VARIANT_CLUSTER / _ROWS / _STREAM */
+    int grid_x;        /* CTAs launched along x (cluster rank, or persistent CTA id) */
+    int grid_y;        /* CTAs along y (tokens for CLUSTER) */
+    int block;         /* threads per CTA */
+    int cluster;       /* CTAs per cluster (1 = none) */
+    int smem_bytes;    /* dynamic shared memory per CTA */
+    int chunks_per_thread; /* 16-byte column chunks each thread owns per row */
+    int sm_count;      /* SMs of the plan's device */
+} mfr_plan_info;
+
+typedef struct mfr_plan_s* mfr_plan_t;
+
+/* 1 when (H, k) is supported, else 0.  Pure: touches no device.
+ * Supported: H % 8 == 0 and 8 <= H <= 16384; 1 <= k <= 16.
+ * Fastest at H in {4096, 8192} and k == 8. */
+int moe_finalize_rmsnorm_supports(int64_t H, int k);
+
+/* Fills *opt with the defaults: enable_pdl = 1, everything else 0. */
+void moe_finalize_rmsnorm_default_options(mfr_options* opt);
+
+/* Creates a plan for T tokens (T >= 0), hidden size H, top-k k and an
+ * expert_out of R rows (R >= 0) on the CURRENT device.  opt may be NULL
+ * (defaults).  Validates the shape, checks the device is compute capability
+ * 10.3, fixes the variant and launch geometry, and allocates the plan's
+ * 4-byte device status word (cleared).  On failure *plan is set to NULL.
+ * A plan is immutable after creation and may be run concurrently on several
+ * streams; they share its status word. */
+int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                              const mfr_options* opt);
+
+/* Enqueues one call of the fused path on `stream`.
+ *  expert_out       device, bf16 [R, H], 16-byte aligned (may be NULL when R == 0)
+ *  permuted_row_of  device, int32 [T, k], 4-byte aligned: row of expert_out for (t, j)
+ *  topk_weights     device, fp32 [T, k], 4-byte aligned: router weights, used as given
+ *  residual_in      device, fp32 [T, H], 16-byte aligned
+ *  residual_out     device, fp32 [T, H], 16-byte aligned; may equal residual_in
+ *                   (in place) but must not otherwise overlap it
+ *  gamma            device, bf16 [H], 16-byte aligned
+ *  eps              finite, >= 0 (eps == 0 with an all-zero row gives NaN, as IEEE says)
+ *  out              device, bf16 [T, H], 16-byte aligned; overlaps no input
+ *  stream           cudaStream_t as void*
+ * A slot whose index lies outside [0, R) adds nothing and sets
+ * MFR_STATUS_BAD_INDEX in the plan's status word (the kernel never reads out
+ * of bounds and never traps).  T == 0 is a no-op returning MFR_OK.
+ * The current device must be the plan's device. */
+int moe_finalize_rmsnorm_run(mfr_plan_t plan,
+                             const void* expert_out, const int32_t* permuted_row_of,
+                             const float* topk_weights, const float* residual_in,
+                             float* residual_out, const void* gamma, float eps,
+                             void* out, void* stream);
+
+/* Waits for `stream`, reads the plan's status word into *device_status
+ * (MFR_STATUS_* bits) and clears it.  Returns MFR_OK or a CUDA error code. */
+int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_status);
+
+/* Copies what the plan decided into *info. */
+int moe_finalize_rmsnorm_plan_info(mfr_plan_t plan, mfr_plan_info* info);
+
+/* Frees the plan and its status word.  NULL is a no-op.  The caller makes
+ * sure no run of this plan is still in flight. */
+void moe_finalize_rmsnorm_destroy(mfr_plan_t plan);
+
+/* Static text for a return code. */
+const char* moe_finalize_rmsnorm_strerror(int code);
+
+/* One-line reason for the last failing call on this thread ("" if none). */
+const char* moe_finalize_rmsnorm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FINALIZE_RMSNORM_H */

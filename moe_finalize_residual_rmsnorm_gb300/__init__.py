@@ -1,0 +1,253 @@
+"""Python binding of libmfr.so — MoE finalize + residual + RMSNorm on GB300.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI (include/moe_finalize_rmsnorm.h).  PyTorch supplies
+device memory and streams.  There is no CPU fallback: if the library is not
+built, importing the binding's entry points raises.
+
+    import moe_finalize_residual_rmsnorm_gb300 as mfr
+    plan = mfr.Plan(T, H, k, R)
+    plan.run(expert_out, permuted_row_of, topk_weights, residual_in,
+             residual_out, gamma, eps, out)          # current torch stream
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from .build import LIBRARY, build as _build_library
+
+__all__ = [
+    "LIBRARY", "MFRError", "Plan", "PlanInfo", "Options", "build", "load_library", "supports",
+    "moe_finalize_residual_rmsnorm", "finalize_residual_rmsnorm_host", "exported_symbols",
+    "VARIANT_AUTO", "VARIANT_CLUSTER", "VARIANT_ROWS", "VARIANT_STREAM", "STATUS_BAD_INDEX",
+    "ERROR_CODES",
+]
+
+MFR_OK = 0
+ERROR_CODES = {
+    1: "MFR_ERR_INVALID_ARG", 2: "MFR_ERR_UNSUPPORTED_SHAPE", 3: "MFR_ERR_MISALIGNED",
+    4: "MFR_ERR_BAD_DEVICE", 5: "MFR_ERR_LAUNCH", 6: "MFR_ERR_CUDA", 7: "MFR_ERR_BAD_INDEX",
+}
+STATUS_BAD_INDEX = 1
+VARIANT_AUTO, VARIANT_CLUSTER, VARIANT_ROWS, VARIANT_STREAM = 0, 1, 2, 3
+VARIANT_NAMES = {VARIANT_CLUSTER: "cluster", VARIANT_ROWS: "rows", VARIANT_STREAM: "stream"}
+
+
+class MFRError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str):
+        self.code = code
+        self.name = ERROR_CODES.get(code, f"code {code}")
+        super().__init__(f"{where}: {self.name}: {detail}")
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("enable_pdl", ctypes.c_int), ("force_variant", ctypes.c_int),
+                ("cluster_size", ctypes.c_int), ("debug_checks", ctypes.c_int)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("grid_x", ctypes.c_int), ("grid_y", ctypes.c_int),
+                ("block", ctypes.c_int), ("cluster", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("chunks_per_thread", ctypes.c_int), ("sm_count", ctypes.c_int)]
+
+    def as_dict(self):
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["variant_name"] = VARIANT_NAMES.get(self.variant, "?")
+        return d
+
+
+# (name, restype, argtypes) of every symbol the header declares
+_VP, _I64, _I, _F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "moe_finalize_rmsnorm_supports": (_I, [_I64, _I]),
+    "moe_finalize_rmsnorm_default_options": (None, [ctypes.POINTER(Options)]),
+    "moe_finalize_rmsnorm_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
+    "moe_finalize_rmsnorm_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _VP]),
+    "moe_finalize_rmsnorm_get_status": (_I, [_VP, _VP, ctypes.POINTER(_I)]),
+    "moe_finalize_rmsnorm_plan_info": (_I, [_VP, ctypes.POINTER(PlanInfo)]),
+    "moe_finalize_rmsnorm_destroy": (None, [_VP]),
+    "moe_finalize_rmsnorm_strerror": (ctypes.c_char_p, [_I]),
+    "moe_finalize_rmsnorm_last_error": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compiles libmfr.so for sm_103a (nvcc) into the package directory."""
+    return _build_library(force=force, verbose=verbose)
+
+
+def load_library():
+    """Loads the in-tree libmfr.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY):
+            raise ImportError(f"{LIBRARY} is missing: build it with "
+                              "moe_finalize_residual_rmsnorm_gb300.build() (nvcc, sm_103a)")
+        lib = ctypes.CDLL(LIBRARY)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def exported_symbols():
+    lib = load_library()
+    return {name for name in SIGNATURES if hasattr(lib, name)}
+
+
+def _check(code: int, where: str):
+    if code != MFR_OK:
+        lib = load_library()
+        detail = lib.moe_finalize_rmsnorm_last_error().decode() or \
+            lib.moe_finalize_rmsnorm_strerror(code).decode()
+        raise MFRError(code, where, detail)
+
+
+def supports(H: int, k: int) -> bool:
+    return bool(load_library().moe_finalize_rmsnorm_supports(H, k))
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Plan:
+    """A plan for T tokens, hidden size H, top-k k and R rows of expert_out on
+    the current CUDA device (C: moe_finalize_rmsnorm_plan)."""
+
+    def __init__(self, T: int, H: int, k: int, R: Optional[int] = None, *, enable_pdl: bool = True,
+                 variant: int = VARIANT_AUTO, cluster_size: int = 0, debug_checks: bool = False):
+        lib = load_library()
+        self._lib = lib
+        self.T, self.H, self.k = int(T), int(H), int(k)
+        self.R = int(T) * int(k) if R is None else int(R)
+        opt = Options(int(bool(enable_pdl)), int(variant), int(cluster_size), int(bool(debug_checks)))
+        h = ctypes.c_void_p()
+        _check(lib.moe_finalize_rmsnorm_plan(ctypes.byref(h), self.T, self.H, self.k, self.R,
+                                             ctypes.byref(opt)), "moe_finalize_rmsnorm_plan")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def info(self) -> dict:
+        inf = PlanInfo()
+        _check(self._lib.moe_finalize_rmsnorm_plan_info(self._h, ctypes.byref(inf)), "plan_info")
+        return inf.as_dict()
+
+    def _validate(self, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, out):
+        import torch
+        T, H, k, R = self.T, self.H, self.k, self.R
+        want = [
+            ("expert_out", expert_out, torch.bfloat16, (R, H)),
+            ("permuted_row_of", permuted_row_of, torch.int32, (T, k)),
+            ("topk_weights", topk_weights, torch.float32, (T, k)),
+            ("residual_in", residual_in, torch.float32, (T, H)),
+            ("residual_out", residual_out, torch.float32, (T, H)),
+            ("gamma", gamma, torch.bfloat16, (H,)),
+            ("out", out, torch.bfloat16, (T, H)),
+        ]
+        for name, t, dt, shape in want:
+            if t.dtype != dt or tuple(t.shape) != shape:
+                raise ValueError(f"{name}: expected {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
+            if not t.is_cuda:
+                raise ValueError(f"{name} must be a CUDA tensor")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+
+    def run(self, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma,
+            eps: float, out, stream=None, *, validate: bool = True) -> None:
+        """Enqueues one call on `stream` (default: torch's current stream).
+        residual_out may be residual_in (in place)."""
+        if validate:
+            self._validate(expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, out)
+        code = self._lib.moe_finalize_rmsnorm_run(
+            self._h, _ptr(expert_out), _ptr(permuted_row_of), _ptr(topk_weights), _ptr(residual_in),
+            _ptr(residual_out), _ptr(gamma), ctypes.c_float(eps), _ptr(out), _stream_handle(stream))
+        _check(code, "moe_finalize_rmsnorm_run")
+
+    def run_ptrs(self, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma,
+                 eps, out, stream) -> int:
+        """Raw-pointer call (ints); returns the C return code unchanged."""
+        return self._lib.moe_finalize_rmsnorm_run(self._h, expert_out, permuted_row_of, topk_weights,
+                                                  residual_in, residual_out, gamma, ctypes.c_float(eps),
+                                                  out, stream)
+
+    def get_status(self, stream=None) -> int:
+        st = ctypes.c_int(0)
+        _check(self._lib.moe_finalize_rmsnorm_get_status(self._h, _stream_handle(stream), ctypes.byref(st)),
+               "moe_finalize_rmsnorm_get_status")
+        return st.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.moe_finalize_rmsnorm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def moe_finalize_residual_rmsnorm(expert_out, permuted_row_of, topk_weights, residual, gamma, eps: float,
+                                  *, residual_out=None, out=None, stream=None, plan: Optional[Plan] = None,
+                                  **plan_kw):
+    """Allocating convenience wrapper: returns (residual_out, out).  With
+    residual_out=residual the update is in place."""
+    import torch
+    T, k = permuted_row_of.shape
+    R, H = expert_out.shape
+    if residual_out is None:
+        residual_out = torch.empty_like(residual)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=residual.device)
+    if plan is None:
+        plan = Plan(T, H, k, R, **plan_kw)
+    plan.run(expert_out, permuted_row_of, topk_weights, residual, residual_out, gamma, eps, out, stream)
+    return residual_out, out
+
+
+def finalize_residual_rmsnorm_host(plan: Plan, host_in: dict, dev: dict, host_out: dict, stream=None):
+    """End-to-end call on host buffers: copies the step's inputs from pinned
+    host memory to the device buffers in `dev`, runs the plan, and copies
+    residual_out and out back into pinned host memory, all on one stream.
+    Returns (h2d_bytes, d2h_bytes)."""
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    h2d = 0
+    with torch.cuda.stream(s):
+        for key in ("expert_out", "permuted_row_of", "topk_weights", "residual", "gamma"):
+            dev[key].copy_(host_in[key], non_blocking=True)
+            h2d += host_in[key].numel() * host_in[key].element_size()
+        plan.run(dev["expert_out"], dev["permuted_row_of"], dev["topk_weights"], dev["residual"],
+                 dev["residual_out"], dev["gamma"], host_in["eps"], dev["out"], s, validate=False)
+        host_out["residual_out"].copy_(dev["residual_out"], non_blocking=True)
+        host_out["out"].copy_(dev["out"], non_blocking=True)
+    d2h = sum(host_out[k].numel() * host_out[k].element_size() for k in ("residual_out", "out"))
+    return h2d, d2h

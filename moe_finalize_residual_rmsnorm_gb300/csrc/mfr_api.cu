@@ -1,0 +1,322 @@
+// Host side of the C ABI declared in include/moe_finalize_rmsnorm.h:
+// argument checks, variant choice, launch geometry, the plan's status word.
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "moe_finalize_rmsnorm.h"
+#include "mfr_internal.h"
+
+struct mfr_plan_s {
+    int64_t T;
+    int64_t H;
+    int64_t R;
+    int k;
+    int device;
+    int sm_count;
+    mfr_options opt;
+    mfr::Launch launch;
+    int* d_status;
+};
+
+namespace {
+
+thread_local char g_last_error[320] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int fail_cuda(int code, const char* what, cudaError_t e) {
+    return fail(code, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// Half-open byte ranges [a, a+na) and [b, b+nb) share a byte.
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// Smallest chunks-per-thread that keeps a CTA within kRowsMaxThreads threads.
+int pick_cpt(int chunks) {
+    for (int cpt : {1, 2, 4})
+        if ((chunks + cpt - 1) / cpt <= mfr::kRowsMaxThreads) return cpt;
+    return 0;
+}
+
+// Cluster size for few tokens: enough CTAs to cover the SMs, a power of two
+// dividing the chunk count, and at least one warp of chunks per CTA.
+int auto_cluster(int64_t T, int chunks, int sm_count) {
+    int c = 1;
+    while (c < 8 && T * c < sm_count) c *= 2;
+    while (c > 1 && (chunks % c != 0 || chunks / c < 32)) c /= 2;
+    return c;
+}
+
+constexpr int64_t kDecodeMaxTokens = 128;
+
+}  // namespace
+
+extern "C" {
+
+int moe_finalize_rmsnorm_supports(int64_t H, int k) {
+    return (H >= 8 && H <= mfr::kMaxH && H % 8 == 0 && k >= 1 && k <= mfr::kMaxK) ? 1 : 0;
+}
+
+void moe_finalize_rmsnorm_default_options(mfr_options* opt) {
+    if (!opt) return;
+    opt->enable_pdl = 1;
+    opt->force_variant = MFR_VARIANT_AUTO;
+    opt->cluster_size = 0;
+    opt->debug_checks = 0;
+}
+
+int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                              const mfr_options* opt) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    *plan = nullptr;
+    if (T < 0 || R < 0) return fail(MFR_ERR_INVALID_ARG, "T and R must be >= 0 (T=%lld R=%lld)",
+                                    (long long)T, (long long)R);
+    if (!moe_finalize_rmsnorm_supports(H, k))
+        return fail(MFR_ERR_UNSUPPORTED_SHAPE,
+                    "unsupported shape H=%lld k=%d (need H %% 8 == 0, 8 <= H <= %d, 1 <= k <= %d)",
+                    (long long)H, k, mfr::kMaxH, mfr::kMaxK);
+    if (R > INT32_MAX) return fail(MFR_ERR_UNSUPPORTED_SHAPE, "R must fit an int32 index");
+    if (T > (int64_t(1) << 26))
+        return fail(MFR_ERR_UNSUPPORTED_SHAPE, "T=%lld exceeds 2^26 tokens per call", (long long)T);
+
+    mfr_options o;
+    moe_finalize_rmsnorm_default_options(&o);
+    if (opt) o = *opt;
+    if (o.force_variant < MFR_VARIANT_AUTO || o.force_variant > MFR_VARIANT_ROWS)
+        return fail(MFR_ERR_INVALID_ARG, "force_variant %d is not available", o.force_variant);
+    if (!(o.cluster_size == 0 || o.cluster_size == 1 || o.cluster_size == 2 ||
+          o.cluster_size == 4 || o.cluster_size == 8 || o.cluster_size == 16))
+        return fail(MFR_ERR_INVALID_ARG, "cluster_size must be 0, 1, 2, 4, 8 or 16");
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { cudaGetLastError(); return fail_cuda(MFR_ERR_BAD_DEVICE, "cudaGetDevice", e); }
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_BAD_DEVICE, "cudaDeviceGetAttribute", e);
+    }
+    if (major != 10 || minor != 3)
+        return fail(MFR_ERR_BAD_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only",
+                    dev, major, minor);
+
+    const int chunks = static_cast<int>(H / 8);
+    mfr::Launch l{};
+    l.pdl = o.enable_pdl ? 1 : 0;
+    l.grid_y = 1;
+    int variant = o.force_variant;
+    int csize = o.cluster_size;
+    if (variant == MFR_VARIANT_AUTO) {
+        if (csize == 0) csize = (T <= kDecodeMaxTokens) ? auto_cluster(T, chunks, sms) : 1;
+        variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
+    } else if (variant == MFR_VARIANT_CLUSTER) {
+        if (csize == 0) csize = auto_cluster(T, chunks, sms);
+        if (csize < 2) csize = 2;
+    } else {
+        csize = 1;
+    }
+    if (chunks % csize != 0)
+        return fail(MFR_ERR_UNSUPPORTED_SHAPE, "cluster of %d CTAs needs H/8 divisible by it (H=%lld)",
+                    csize, (long long)H);
+    const int cta_chunks = chunks / csize;
+    l.variant = variant;
+    l.cluster = csize;
+    l.cpt = pick_cpt(cta_chunks);
+    if (l.cpt == 0) return fail(MFR_ERR_UNSUPPORTED_SHAPE, "H=%lld too wide", (long long)H);
+    l.block = round_up((cta_chunks + l.cpt - 1) / l.cpt, 32);
+    l.grid_x = static_cast<int>(T > 0 ? T * csize : csize);
+    l.smem_bytes = 0;
+
+    if ((e = mfr::rows_prepare(l)) != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
+    }
+    if (csize > 1) {
+        int nclusters = 0;
+        e = mfr::rows_max_active_clusters(l, &nclusters);
+        if (e != cudaSuccess || nclusters < 1) {
+            cudaGetLastError();
+            return fail(MFR_ERR_UNSUPPORTED_SHAPE, "a cluster of %d CTAs x %d threads cannot be resident",
+                        csize, l.block);
+        }
+    }
+
+    int* status = nullptr;
+    if ((e = cudaMalloc(&status, sizeof(int))) != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_CUDA, "cudaMalloc(status)", e);
+    }
+    if ((e = cudaMemset(status, 0, sizeof(int))) != cudaSuccess) {
+        cudaFree(status);
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_CUDA, "cudaMemset(status)", e);
+    }
+    mfr_plan_s* p = new (std::nothrow) mfr_plan_s{};
+    if (!p) {
+        cudaFree(status);
+        return fail(MFR_ERR_CUDA, "out of host memory");
+    }
+    p->T = T;
+    p->H = H;
+    p->R = R;
+    p->k = k;
+    p->device = dev;
+    p->sm_count = sms;
+    p->opt = o;
+    p->launch = l;
+    p->d_status = status;
+    *plan = p;
+    return MFR_OK;
+}
+
+int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
+                             const float* topk_weights, const float* residual_in, float* residual_out,
+                             const void* gamma, float eps, void* out, void* stream) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    const int64_t T = plan->T, H = plan->H, R = plan->R;
+    const int k = plan->k;
+    if (T == 0) return MFR_OK;
+    if (!permuted_row_of || !topk_weights || !residual_in || !residual_out || !gamma || !out ||
+        (R > 0 && !expert_out))
+        return fail(MFR_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!std::isfinite(eps) || eps < 0.f)
+        return fail(MFR_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (!aligned(expert_out, 16) || !aligned(residual_in, 16) || !aligned(residual_out, 16) ||
+        !aligned(gamma, 16) || !aligned(out, 16))
+        return fail(MFR_ERR_MISALIGNED, "expert_out, residual_in, residual_out, gamma and out must be "
+                                        "16-byte aligned");
+    if (!aligned(permuted_row_of, 4) || !aligned(topk_weights, 4))
+        return fail(MFR_ERR_MISALIGNED, "permuted_row_of and topk_weights must be 4-byte aligned");
+
+    const size_t n_res = static_cast<size_t>(T * H) * sizeof(float);
+    const size_t n_out = static_cast<size_t>(T * H) * 2;
+    const size_t n_e = static_cast<size_t>(R * H) * 2;
+    const size_t n_tk = static_cast<size_t>(T * k) * 4;
+    if (residual_out != residual_in && overlaps(residual_out, n_res, residual_in, n_res))
+        return fail(MFR_ERR_INVALID_ARG, "residual_out partially overlaps residual_in");
+    if (overlaps(residual_out, n_res, expert_out, n_e) || overlaps(residual_out, n_res, permuted_row_of, n_tk) ||
+        overlaps(residual_out, n_res, topk_weights, n_tk) || overlaps(residual_out, n_res, gamma, H * 2))
+        return fail(MFR_ERR_INVALID_ARG, "residual_out overlaps an input");
+    if (overlaps(out, n_out, expert_out, n_e) || overlaps(out, n_out, permuted_row_of, n_tk) ||
+        overlaps(out, n_out, topk_weights, n_tk) || overlaps(out, n_out, residual_in, n_res) ||
+        overlaps(out, n_out, residual_out, n_res) || overlaps(out, n_out, gamma, H * 2))
+        return fail(MFR_ERR_INVALID_ARG, "out overlaps another argument");
+
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { cudaGetLastError(); return fail_cuda(MFR_ERR_CUDA, "cudaGetDevice", e); }
+    if (dev != plan->device)
+        return fail(MFR_ERR_INVALID_ARG, "current device %d is not the plan's device %d", dev, plan->device);
+
+    mfr::Params p{};
+    p.expert_out = static_cast<const uint16_t*>(expert_out);
+    p.permuted_row_of = permuted_row_of;
+    p.topk_weights = topk_weights;
+    p.residual_in = residual_in;
+    p.residual_out = residual_out;
+    p.gamma = static_cast<const uint16_t*>(gamma);
+    p.out = static_cast<uint16_t*>(out);
+    p.status = plan->d_status;
+    p.T = T;
+    p.R = R;
+    p.H = static_cast<int>(H);
+    p.k = k;
+    p.eps = eps;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = mfr::rows_launch(p, plan->launch, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_LAUNCH, "kernel launch", e);
+    }
+    if (plan->opt.debug_checks) {
+        int st = 0;
+        const int rc = moe_finalize_rmsnorm_get_status(plan, stream, &st);
+        if (rc != MFR_OK) return rc;
+        if (st & MFR_STATUS_BAD_INDEX)
+            return fail(MFR_ERR_BAD_INDEX, "a permuted_row_of entry was outside [0, %lld)", (long long)R);
+    }
+    return MFR_OK;
+}
+
+int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_status) {
+    g_last_error[0] = '\0';
+    if (!plan || !device_status) return fail(MFR_ERR_INVALID_ARG, "plan and device_status must not be NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, plan->d_status, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(plan->d_status, 0, sizeof(int), s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_CUDA, "reading the status word", e);
+    }
+    *device_status = h;
+    return MFR_OK;
+}
+
+int moe_finalize_rmsnorm_plan_info(mfr_plan_t plan, mfr_plan_info* info) {
+    if (!plan || !info) return fail(MFR_ERR_INVALID_ARG, "plan and info must not be NULL");
+    const mfr::Launch& l = plan->launch;
+    info->variant = l.variant;
+    info->grid_x = l.grid_x;
+    info->grid_y = l.grid_y;
+    info->block = l.block;
+    info->cluster = l.cluster;
+    info->smem_bytes = l.smem_bytes;
+    info->chunks_per_thread = l.cpt;
+    info->sm_count = plan->sm_count;
+    return MFR_OK;
+}
+
+void moe_finalize_rmsnorm_destroy(mfr_plan_t plan) {
+    if (!plan) return;
+    if (plan->d_status) {
+        cudaFree(plan->d_status);
+        cudaGetLastError();
+    }
+    delete plan;
+}
+
+const char* moe_finalize_rmsnorm_strerror(int code) {
+    switch (code) {
+        case MFR_OK: return "ok";
+        case MFR_ERR_INVALID_ARG: return "invalid argument";
+        case MFR_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MFR_ERR_MISALIGNED: return "misaligned pointer";
+        case MFR_ERR_BAD_DEVICE: return "unsupported or unavailable device (needs sm_103)";
+        case MFR_ERR_LAUNCH: return "kernel launch failed";
+        case MFR_ERR_CUDA: return "CUDA runtime error";
+        case MFR_ERR_BAD_INDEX: return "permuted_row_of entry out of range";
+        default: return "unknown error code";
+    }
+}
+
+const char* moe_finalize_rmsnorm_last_error(void) { return g_last_error; }
+
+}  // extern "C"

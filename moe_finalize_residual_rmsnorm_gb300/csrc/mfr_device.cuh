@@ -1,0 +1,85 @@
+// Device helpers shared by the kernels of this library (sm_103a only).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "moe_finalize_rmsnorm.h"
+
+namespace mfr {
+
+// ---- programmatic dependent launch ----------------------------------------
+// Wait until every kernel this one depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialization) has finished
+// and its writes are visible.  A no-op for an ordinary launch.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel in the stream start its own prologue.  It still waits
+// for this whole grid before reading what this grid writes.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- loads and stores --------------------------------------------------------
+// 16 bytes of read-only, read-once data: skip L1 and ask L2 for a 256-byte
+// prefetch (the rows are long and contiguous).  volatile keeps it after
+// pdl_wait().
+__device__ __forceinline__ uint4 ld_stream_u4(const void* ptr) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
+
+// 16 bytes of data this kernel may also write (the residual, in place).
+__device__ __forceinline__ float4 ld_once_f4(const float* ptr) {
+    float4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(ptr));
+    return v;
+}
+
+__device__ __forceinline__ void st_f4(float* ptr, float4 v) {
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(ptr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void st_u4(void* ptr, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// ---- bf16 -----------------------------------------------------------------------
+// Element e (0..7) of 8 packed bf16 values, widened exactly to fp32.
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// Two fp32 values rounded to nearest-even bf16, packed low = a, high = b.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---- reductions ------------------------------------------------------------------
+// Butterfly sum over the 32 lanes.  Each level adds a value to its partner's,
+// and fp32 addition is commutative, so every lane ends with the same bits.
+__device__ __forceinline__ float warp_allreduce_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+    return v;
+}
+
+}  // namespace mfr

@@ -1,0 +1,49 @@
+// Declarations shared by the host ABI (mfr_api.cu) and the kernel files.
+// Not part of the public ABI; see include/moe_finalize_rmsnorm.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mfr {
+
+// Everything a kernel needs for one call; passed by value.
+struct Params {
+    const uint16_t* expert_out;     // bf16 bits [R, H]
+    const int32_t* permuted_row_of; // [T, k]
+    const float* topk_weights;      // [T, k]
+    const float* residual_in;       // [T, H]
+    float* residual_out;            // [T, H]
+    const uint16_t* gamma;          // bf16 bits [H]
+    uint16_t* out;                  // bf16 bits [T, H]
+    int* status;                    // device status word (MFR_STATUS_* bits)
+    int64_t T;
+    int64_t R;
+    int H;
+    int k;
+    float eps;
+};
+
+// Launch geometry fixed by the plan.
+struct Launch {
+    int variant;      // MFR_VARIANT_*
+    int grid_x;
+    int grid_y;
+    int block;
+    int cluster;      // CTAs per cluster along x (1 = no cluster)
+    int smem_bytes;   // dynamic shared memory
+    int cpt;          // 16-byte chunks per thread per row
+    int pdl;          // programmatic stream serialization
+};
+
+constexpr int kMaxK = 16;         // slots per token
+constexpr int kMaxH = 16384;      // hidden size
+constexpr int kRowsMaxThreads = 512;
+
+// mfr_rows.cu: one CTA (or one cluster of CTAs) per token.
+bool rows_supported_cpt(int cpt);
+cudaError_t rows_prepare(const Launch& l);   // per-kernel attributes (cluster > 8)
+cudaError_t rows_max_active_clusters(const Launch& l, int* n);
+cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s);
+
+}  // namespace mfr

@@ -1,0 +1,249 @@
+// Register-gather kernel: one CTA per token (MFR_VARIANT_ROWS), or a
+// cluster of C CTAs per token that split the hidden dimension and combine
+// their sums of squares through distributed shared memory
+// (MFR_VARIANT_CLUSTER).
+//
+// Per token t, for the columns this CTA owns:
+//   prologue  : slot indices and weights of t, gamma        (before the PDL wait)
+//   wait      : the producer of expert_out / residual_in has finished
+//   gather    : k rows of expert_out, 16 bytes per load, all loads of a slot
+//               group issued before any is used
+//   accumulate: acc = fma(w_j, e_j, acc) for j = 0..k-1 in slot order
+//               (FlashInfer PR 5319 analysis, section 1: FP32 FMA, BF16 at the end)
+//   residual  : x = residual_in + acc, written to residual_out
+//               (FlashInfer PR 4730 analysis, section 2: sum, residual, RMSNorm fused)
+//   reduce    : sum of x^2 — per thread in column order, a warp butterfly,
+//               warps in index order, then (cluster) CTAs in rank order
+//               through DSMEM (PR 4730 analysis, section 2: cluster exchange)
+//   normalise : y = (x * rsqrt(ss / H + eps)) * gamma, rounded to bf16
+// Every reduction order is fixed by (H, k, launch geometry), so a plan gives
+// bitwise-identical results on every run.
+#include <cooperative_groups.h>
+
+#include "mfr_device.cuh"
+#include "mfr_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace mfr {
+namespace {
+
+// CPT: 16-byte column chunks per thread per row; SG: slots gathered together.
+template <int CPT, int SG>
+__global__ void __launch_bounds__(kRowsMaxThreads)
+rows_kernel(const Params p, const int csize)
+{
+    const int tid = threadIdx.x;
+    const int nthreads = blockDim.x;
+    const int64_t t = blockIdx.x / csize;
+    const int rank = static_cast<int>(blockIdx.x - t * csize);
+    const int nck = (p.H >> 3) / csize;        // chunks of this CTA
+    const int64_t col0 = static_cast<int64_t>(rank) * nck * 8;
+
+    __shared__ int s_row[kMaxK];
+    __shared__ float s_w[kMaxK];
+    __shared__ float s_warp[kRowsMaxThreads / 32];
+    __shared__ float s_cta[16];
+
+    if (csize > 1)
+        cg::this_cluster().barrier_arrive();   // peers write s_cta only after all CTAs started
+
+    // ---- prologue: inputs that the producing kernel does not write --------
+    if (tid < p.k) {
+        const int32_t r = p.permuted_row_of[t * p.k + tid];
+        const bool ok = (r >= 0) && (static_cast<int64_t>(r) < p.R);
+        if (!ok && rank == 0)
+            atomicOr(p.status, MFR_STATUS_BAD_INDEX);
+        s_row[tid] = ok ? r : -1;
+        s_w[tid] = p.topk_weights[t * p.k + tid];
+    }
+    uint4 g[CPT];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int c = tid + i * nthreads;
+        g[i] = (c < nck) ? *reinterpret_cast<const uint4*>(p.gamma + col0 + c * 8)
+                         : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+
+    pdl_wait();
+
+    // ---- residual row and the k expert rows ---------------------------------
+    const float* res_in = p.residual_in + t * p.H + col0;
+    float res[CPT][8];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int c = tid + i * nthreads;
+        if (c < nck) {
+            const float4 a = ld_once_f4(res_in + c * 8);
+            const float4 b = ld_once_f4(res_in + c * 8 + 4);
+            res[i][0] = a.x; res[i][1] = a.y; res[i][2] = a.z; res[i][3] = a.w;
+            res[i][4] = b.x; res[i][5] = b.y; res[i][6] = b.z; res[i][7] = b.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) res[i][q] = 0.f;
+        }
+    }
+
+    float acc[CPT][8];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[i][q] = 0.f;
+
+    for (int j0 = 0; j0 < p.k; j0 += SG) {
+        uint4 v[SG][CPT];
+#pragma unroll
+        for (int s = 0; s < SG; ++s) {
+            const int j = j0 + s;
+            const int r = (j < p.k) ? s_row[j] : -1;
+            const uint16_t* row = p.expert_out + static_cast<int64_t>(r < 0 ? 0 : r) * p.H + col0;
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                const int c = tid + i * nthreads;
+                v[s][i] = (r >= 0 && c < nck) ? ld_stream_u4(row + c * 8) : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < SG; ++s) {
+            const int j = j0 + s;
+            if (j < p.k && s_row[j] >= 0) {
+                const float wj = s_w[j];
+#pragma unroll
+                for (int i = 0; i < CPT; ++i) {
+                    float e[8];
+                    unpack8(v[s][i], e);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[i][q] = __fmaf_rn(wj, e[q], acc[i][q]);
+                }
+            }
+        }
+    }
+
+    // ---- x = residual + acc; write the residual; sum of squares ------------
+    float* res_out = p.residual_out + t * p.H + col0;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int c = tid + i * nthreads;
+        if (c < nck) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                acc[i][q] = res[i][q] + acc[i][q];
+                ss = __fmaf_rn(acc[i][q], acc[i][q], ss);
+            }
+            st_f4(res_out + c * 8, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+            st_f4(res_out + c * 8 + 4, make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]));
+        }
+    }
+
+    ss = warp_allreduce_sum(ss);
+    if ((tid & 31) == 0)
+        s_warp[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    const int nwarps = nthreads >> 5;
+    for (int w = 0; w < nwarps; ++w)
+        tot += s_warp[w];
+
+    if (csize > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.barrier_wait();                      // all CTAs have started
+        if (tid < csize) {
+            float* dst = cluster.map_shared_rank(&s_cta[rank], tid);
+            *dst = tot;
+        }
+        cluster.barrier_arrive();
+        cluster.barrier_wait();                      // every partial has landed
+        tot = 0.f;
+        for (int r = 0; r < csize; ++r)
+            tot += s_cta[r];
+    }
+
+    pdl_launch_dependents();
+
+    // ---- y = (x * inv) * gamma -> bf16 ----------------------------------------
+    const float inv = rsqrtf(tot / static_cast<float>(p.H) + p.eps);
+    uint16_t* out = p.out + t * p.H + col0;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int c = tid + i * nthreads;
+        if (c < nck) {
+            float gf[8];
+            unpack8(g[i], gf);
+            uint4 o;
+            o.x = pack_bf16x2(acc[i][0] * inv * gf[0], acc[i][1] * inv * gf[1]);
+            o.y = pack_bf16x2(acc[i][2] * inv * gf[2], acc[i][3] * inv * gf[3]);
+            o.z = pack_bf16x2(acc[i][4] * inv * gf[4], acc[i][5] * inv * gf[5]);
+            o.w = pack_bf16x2(acc[i][6] * inv * gf[6], acc[i][7] * inv * gf[7]);
+            st_u4(out + c * 8, o);
+        }
+    }
+}
+
+using RowsKernel = void (*)(const Params, const int);
+
+RowsKernel rows_kernel_for(int cpt) {
+    switch (cpt) {
+        case 1: return rows_kernel<1, 8>;
+        case 2: return rows_kernel<2, 8>;
+        case 4: return rows_kernel<4, 4>;
+        default: return nullptr;
+    }
+}
+
+void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attrs, const Launch& l,
+                 cudaStream_t s) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = dim3(static_cast<unsigned>(l.grid_x), static_cast<unsigned>(l.grid_y), 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(l.block), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(l.smem_bytes);
+    cfg.stream = s;
+    int n = 0;
+    if (l.cluster > 1) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = static_cast<unsigned>(l.cluster);
+        attrs[n].val.clusterDim.y = 1;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (l.pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = static_cast<unsigned>(n);
+}
+
+}  // namespace
+
+bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt) != nullptr; }
+
+cudaError_t rows_prepare(const Launch& l) {
+    RowsKernel k = rows_kernel_for(l.cpt);
+    if (!k) return cudaErrorInvalidValue;
+    if (l.cluster > 8)
+        return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return cudaSuccess;
+}
+
+cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
+    RowsKernel k = rows_kernel_for(l.cpt);
+    if (!k) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attrs[2];
+    fill_config(cfg, attrs, l, nullptr);
+    return cudaOccupancyMaxActiveClusters(n, k, &cfg);
+}
+
+cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s) {
+    RowsKernel k = rows_kernel_for(l.cpt);
+    if (!k) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attrs[2];
+    fill_config(cfg, attrs, l, s);
+    return cudaLaunchKernelEx(&cfg, k, p, l.cluster);
+}
+
+}  // namespace mfr

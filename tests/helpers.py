@@ -1,0 +1,70 @@
+"""Shared test helpers: tolerances, comparisons, host copies.  No finalize
+arithmetic lives here."""
+import numpy as np
+import torch
+
+import oracle
+
+# FP32 residual: |gpu - oracle| <= max(REL * |oracle|, ABS) per element
+RES_REL = 1e-6
+RES_ABS = 1e-6
+# bf16 output: at most this many units in the last place apart
+OUT_ULP = 1
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().numpy()
+
+
+def bf16_ordered(b: np.ndarray) -> np.ndarray:
+    """Maps bf16 bit patterns to integers whose order is the value order;
+    +0 and -0 both map to 0."""
+    b = b.astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def bf16_is_nan(b: np.ndarray) -> np.ndarray:
+    return ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+
+
+def bf16_ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    d = np.abs(bf16_ordered(a) - bf16_ordered(b)).astype(np.float64)
+    na, nb = bf16_is_nan(a), bf16_is_nan(b)
+    d[na & nb] = 0
+    d[na ^ nb] = np.inf
+    return d
+
+
+def assert_residual_close(got: np.ndarray, want: np.ndarray, what="residual_out"):
+    got = np.asarray(got, dtype=np.float32)
+    want = np.asarray(want, dtype=np.float32)
+    both_nan = np.isnan(got) & np.isnan(want)
+    err = np.abs(got.astype(np.float64) - want.astype(np.float64))
+    tol = np.maximum(RES_REL * np.abs(want.astype(np.float64)), RES_ABS)
+    bad = ~both_nan & ~(err <= tol) & ~(got == want)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance; first at {tuple(i)}: "
+                             f"got {got[tuple(i)]!r} want {want[tuple(i)]!r}")
+
+
+def assert_out_close(got_bits: np.ndarray, want_bits: np.ndarray, what="out", ulp=OUT_ULP):
+    d = bf16_ulp_distance(got_bits, want_bits)
+    if not np.all(d <= ulp):
+        i = np.argwhere(~(d <= ulp))[0]
+        raise AssertionError(f"{what}: {(~(d <= ulp)).sum()} elements beyond {ulp} ulp; first at {tuple(i)}: "
+                             f"got 0x{int(got_bits[tuple(i)]):04x} want 0x{int(want_bits[tuple(i)]):04x}")
+
+
+def oracle_on(inputs: dict, tokens=None, residual=None):
+    """Runs the oracle on host copies of the inputs (optionally on a subset
+    of tokens).  Returns (residual_out, out_bits, bad_slots)."""
+    res = f32(inputs["residual"] if residual is None else residual)
+    return oracle.finalize_residual_rmsnorm(
+        bf16_bits(inputs["expert_out"]), inputs["permuted_row_of"].cpu().numpy(),
+        f32(inputs["topk_weights"]), res, bf16_bits(inputs["gamma"]), inputs["eps"], tokens=tokens)

@@ -1,0 +1,261 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small cases compare every element; the full-size workloads, in the launch
+configuration the benchmark times, compare sampled tokens.  Bars:
+residual_out within max(1e-6 * |oracle|, 1e-6) per element (in practice
+bit-equal: both sides do the same FP32 operations), out within 1 bf16 ulp,
+and repeated runs bitwise identical.  Every output buffer sits between guard
+regions that must come back untouched.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import moe_finalize_residual_rmsnorm_gb300 as mfr
+import workloads as W
+from helpers import (assert_out_close, assert_residual_close, bf16_bits, f32, oracle_on)
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 256  # elements of guard on each side of every output
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    mfr.build()
+    mfr.load_library()
+
+
+def guarded(shape, dtype, fill):
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * GUARD,), fill, dtype=dtype, device="cuda")
+    return buf, buf[GUARD:GUARD + n].view(*shape)
+
+
+def check_guards(buf, fill):
+    head, tail = buf[:GUARD], buf[-GUARD:]
+    assert torch.equal(head, torch.full_like(head, fill)) and torch.equal(tail, torch.full_like(tail, fill)), \
+        "a kernel wrote outside its output"
+
+
+def run_gpu(inp, plan_kw=None, in_place=False, residual=None):
+    """Runs one call through the binding (C ABI) with guarded outputs.
+    Returns host copies (residual_out f32, out bf16 bits) and the plan."""
+    e, idx, w, g = inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], inp["gamma"]
+    res = inp["residual"] if residual is None else residual
+    T, k = idx.shape
+    R, H = e.shape
+    plan = mfr.Plan(T, H, k, R, **(plan_kw or {}))
+    ob, out = guarded((T, H), torch.bfloat16, -7.0)
+    if in_place:
+        rb, rout = guarded((T, H), torch.float32, -3.0)
+        rout.copy_(res)
+        rin = rout
+    else:
+        rb, rout = guarded((T, H), torch.float32, -3.0)
+        rin = res
+    plan.run(e, idx, w, rin, rout, g, inp["eps"], out)
+    torch.cuda.synchronize()
+    check_guards(ob, -7.0)
+    check_guards(rb, -3.0)
+    return f32(rout), bf16_bits(out), plan
+
+
+def compare_full(inp, plan_kw=None, in_place=False):
+    want_res, want_out, bad = oracle_on(inp)
+    got_res, got_out, plan = run_gpu(inp, plan_kw, in_place)
+    assert_residual_close(got_res, want_res)
+    assert_out_close(got_out, want_out)
+    status = plan.get_status()
+    assert bool(status & mfr.STATUS_BAD_INDEX) == (bad > 0)
+    return got_res, want_res, got_out, want_out, plan
+
+
+def inputs_for(T, H, k, R=None, seed=0, E=None, **kw):
+    wl = W.Workload(f"case_T{T}_H{H}_k{k}", T=T, H=H, k=k, E=E or max(2 * k, 16), seed=seed,
+                    extra_rows=0 if R is None else R - T * k, **kw)
+    return W.make_inputs(wl, "cuda")
+
+
+# --- small cases, every element -----------------------------------------------
+
+def test_tiny_ref_auto_plan_is_bit_exact_on_the_residual():
+    inp = W.make_inputs(W.TINY_REF, "cuda")
+    got_res, want_res, got_out, want_out, plan = compare_full(inp)
+    assert np.array_equal(got_res.view(np.uint32), want_res.view(np.uint32))
+    # at most a small share of outputs sit one ulp away (rounding near ties)
+    assert np.mean(got_out != want_out) < 0.02
+
+
+@pytest.mark.parametrize("variant,cluster", [(mfr.VARIANT_ROWS, 0), (mfr.VARIANT_CLUSTER, 2),
+                                             (mfr.VARIANT_CLUSTER, 4), (mfr.VARIANT_CLUSTER, 8),
+                                             (mfr.VARIANT_CLUSTER, 16)])
+@pytest.mark.parametrize("pdl", [True, False])
+def test_tiny_ref_every_variant(variant, cluster, pdl):
+    inp = W.make_inputs(W.TINY_REF, "cuda")
+    _, _, _, _, plan = compare_full(inp, dict(variant=variant, cluster_size=cluster, enable_pdl=pdl))
+    info = plan.info()
+    assert info["variant"] == variant
+    if variant == mfr.VARIANT_CLUSTER:
+        assert info["cluster"] == cluster
+
+
+@pytest.mark.parametrize("T", W.DECODE_TOKENS + (3, 5, 7, 100))
+def test_decode_sweep_auto_plan(T):
+    compare_full(W.make_inputs(W.decode(T), "cuda", T=T))
+
+
+@pytest.mark.parametrize("H", [8, 24, 136, 1024, 4104, 8192, 12288, 16384])
+@pytest.mark.parametrize("k", [1, 5, 8, 16])
+def test_shapes_with_ragged_tails(H, k):
+    T = 5
+    inp = inputs_for(T, H, k, R=T * k + 3, seed=H + k)
+    compare_full(inp)
+    if H % 64 == 0 and H >= 1024:
+        compare_full(inp, dict(variant=mfr.VARIANT_CLUSTER, cluster_size=8))
+
+
+def test_in_place_residual():
+    inp = W.make_inputs(W.decode(16), "cuda")
+    for kw in (dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=4)):
+        compare_full(inp, kw, in_place=True)
+
+
+def test_out_of_range_indices_add_nothing_and_raise_the_status_bit():
+    inp = inputs_for(6, 1024, 8, seed=3)
+    idx = inp["permuted_row_of"].clone()
+    R = inp["expert_out"].shape[0]
+    idx[0, 0] = -1
+    idx[2, 7] = R
+    idx[5, 3] = 2**31 - 1
+    idx[4, 4] = -(2**31)
+    inp["permuted_row_of"] = idx
+    for kw in (dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=2)):
+        compare_full(inp, kw)
+
+
+def test_debug_checks_turn_a_bad_index_into_an_error():
+    inp = inputs_for(2, 512, 8, seed=4)
+    inp["permuted_row_of"][1, 1] = -5
+    with pytest.raises(mfr.MFRError) as ei:
+        run_gpu(inp, dict(debug_checks=True))
+    assert ei.value.code == 7
+
+
+def test_duplicate_rows_and_special_weights():
+    inp = inputs_for(4, 2048, 8, seed=5)
+    idx = inp["permuted_row_of"].clone()
+    idx[0, :] = idx[0, 0]                 # one row eight times
+    idx[1, 1::2] = idx[1, 0::2]
+    w = inp["topk_weights"].clone()
+    w[2] = torch.tensor([0.0, -0.0, -1.5, 2.0**-30, 3.0e5, -1e-20, 0.25, 1.0])
+    w[3] = -w[3]
+    inp["permuted_row_of"], inp["topk_weights"] = idx, w
+    compare_full(inp)
+
+
+def test_nan_inf_and_zero_rows_propagate_like_ieee():
+    inp = inputs_for(5, 1024, 4, seed=6)
+    e = inp["expert_out"]
+    idx = inp["permuted_row_of"]
+    e[idx[0, 1]] = float("nan")
+    e[idx[1, 2], 17] = float("inf")
+    # token 2: every contribution cancels the residual exactly -> all-zero x
+    inp["topk_weights"][2] = torch.tensor([1.0, 0.0, 0.0, 0.0])
+    inp["residual"][2] = -e[idx[2, 0]].float()
+    inp["eps"] = 0.0
+    got_res, want_res, got_out, want_out, _ = compare_full(inp)
+    assert np.isnan(got_res[0]).all()
+    assert np.all(got_res[2] == 0)
+
+
+def test_large_magnitudes_and_tiny_eps():
+    inp = W.make_inputs(W.STRESS, "cuda", T=24)
+    compare_full(inp)
+    inp["eps"] = 1e-12
+    compare_full(inp)
+
+
+def test_zero_tokens_is_a_no_op():
+    plan = mfr.Plan(0, 4096, 8, 0)
+    z = torch.empty(0, device="cuda")
+    code = plan.run_ptrs(0, 0, 0, 0, 0, 0, 1e-6, 0, 0)
+    assert code == 0
+    del z
+
+
+def test_repeated_runs_are_bitwise_identical():
+    inp = W.make_inputs(W.PREFILL, "cuda", T=1000)
+    a = run_gpu(inp)
+    b = run_gpu(inp)
+    assert np.array_equal(a[0].view(np.uint32), b[0].view(np.uint32))
+    assert np.array_equal(a[1], b[1])
+
+
+# --- argument checks on a real device --------------------------------------------
+
+def test_run_rejects_bad_arguments_without_launching():
+    inp = inputs_for(4, 1024, 8, seed=7)
+    T, H, k, R = 4, 1024, 8, 32
+    plan = mfr.Plan(T, H, k, R)
+    e, idx, w, res, g = (inp[n] for n in ("expert_out", "permuted_row_of", "topk_weights", "residual", "gamma"))
+    rout = torch.empty_like(res)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    p = lambda t: t.data_ptr()  # noqa: E731
+    s = torch.cuda.current_stream().cuda_stream
+    ok = (p(e), p(idx), p(w), p(res), p(rout), p(g), 1e-6, p(out), s)
+    assert plan.run_ptrs(*ok) == 0
+    bad = list(ok); bad[0] = p(e) + 2                                  # misaligned expert_out
+    assert plan.run_ptrs(*bad) == 3
+    bad = list(ok); bad[7] = p(out) + 8                                # misaligned out
+    assert plan.run_ptrs(*bad) == 3
+    bad = list(ok); bad[1] = p(idx) + 2                                # misaligned index map
+    assert plan.run_ptrs(*bad) == 3
+    for eps in (-1.0, float("nan"), float("inf")):
+        bad = list(ok); bad[6] = eps
+        assert plan.run_ptrs(*bad) == 1
+    bad = list(ok); bad[7] = p(res)                                    # out aliases residual_in
+    assert plan.run_ptrs(*bad) == 1
+    bad = list(ok); bad[4] = p(res) + 16                               # partial residual overlap
+    assert plan.run_ptrs(*bad) == 1
+    bad = list(ok); bad[2] = 0                                         # null weights
+    assert plan.run_ptrs(*bad) == 1
+    torch.cuda.synchronize()
+    assert plan.get_status() == 0
+
+
+# --- full sizes, in the benchmark's launch configuration -----------------------------
+
+FULL = [W.PREFILL, W.wide(4096), W.wide(8192), W.STRESS]
+
+
+@pytest.mark.parametrize("wl", FULL, ids=lambda w: w.name)
+def test_full_size_sampled_tokens(wl):
+    inp = W.make_inputs(wl, "cuda")
+    T = wl.T
+    plan = mfr.Plan(T, wl.H, wl.k, wl.R)          # the benchmark's plan: auto variant, PDL on
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(inp["residual"])
+    plan.run(inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], inp["residual"], rout,
+             inp["gamma"], inp["eps"], out)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(wl.T)
+    tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=62, replace=False)]))
+    want_res, want_out, bad = oracle_on(inp, tokens=tokens)
+    assert bad == 0
+    assert_residual_close(f32(rout)[tokens], want_res)
+    assert_out_close(bf16_bits(out)[tokens], want_out)
+    assert plan.get_status() == 0
+    if wl is W.STRESS:
+        # run twice more; every byte of both outputs must repeat
+        out2, rout2 = torch.empty_like(out), torch.empty_like(rout)
+        for _ in range(2):
+            plan.run(inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], inp["residual"], rout2,
+                     inp["gamma"], inp["eps"], out2)
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+            assert torch.equal(rout.view(torch.int32), rout2.view(torch.int32))
