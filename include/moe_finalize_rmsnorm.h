@@ -65,6 +65,8 @@ extern "C" {
 
 /* ---- bits of the device status word ------------------------------------- */
 #define MFR_STATUS_BAD_INDEX      1  /* some slot index was outside [0, R); that slot added 0 */
+#define MFR_STATUS_TIMEOUT        2  /* a bounded on-chip wait gave up (never expected); the
+                                        outputs of that call are not valid */
 
 /* ---- kernel variants ---------------------------------------------------- */
 #define MFR_VARIANT_AUTO          0  /* chosen from (T, H, k, device) only  */
@@ -142,6 +144,12 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan,
 /* Waits for `stream`, reads the plan's status word into *device_status
  * (MFR_STATUS_* bits) and clears it.  Returns MFR_OK or a CUDA error code. */
 int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_status);
+
+/* Enqueues an EMPTY kernel with exactly the plan's launch geometry (grid,
+ * block, cluster, dynamic shared memory, PDL attribute) that only performs the
+ * dependent-launch wait and trigger.  Benchmarks time it to get the launch
+ * floor of a call.  Touches no memory.  T == 0 is a no-op. */
+int moe_finalize_rmsnorm_launch_floor(mfr_plan_t plan, void* stream);
 
 /* Copies what the plan decided into *info. */
 int moe_finalize_rmsnorm_plan_info(mfr_plan_t plan, mfr_plan_info* info);

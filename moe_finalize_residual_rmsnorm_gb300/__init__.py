@@ -31,6 +31,7 @@ ERROR_CODES = {
     4: "MFR_ERR_BAD_DEVICE", 5: "MFR_ERR_LAUNCH", 6: "MFR_ERR_CUDA", 7: "MFR_ERR_BAD_INDEX",
 }
 STATUS_BAD_INDEX = 1
+STATUS_TIMEOUT = 2
 VARIANT_AUTO, VARIANT_CLUSTER, VARIANT_ROWS, VARIANT_STREAM = 0, 1, 2, 3
 VARIANT_NAMES = {VARIANT_CLUSTER: "cluster", VARIANT_ROWS: "rows", VARIANT_STREAM: "stream"}
 
@@ -67,6 +68,7 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _VP]),
     "moe_finalize_rmsnorm_get_status": (_I, [_VP, _VP, ctypes.POINTER(_I)]),
     "moe_finalize_rmsnorm_plan_info": (_I, [_VP, ctypes.POINTER(PlanInfo)]),
+    "moe_finalize_rmsnorm_launch_floor": (_I, [_VP, _VP]),
     "moe_finalize_rmsnorm_destroy": (None, [_VP]),
     "moe_finalize_rmsnorm_strerror": (ctypes.c_char_p, [_I]),
     "moe_finalize_rmsnorm_last_error": (ctypes.c_char_p, []),
@@ -190,6 +192,11 @@ class Plan:
         return self._lib.moe_finalize_rmsnorm_run(self._h, expert_out, permuted_row_of, topk_weights,
                                                   residual_in, residual_out, gamma, ctypes.c_float(eps),
                                                   out, stream)
+
+    def launch_floor(self, stream=None) -> None:
+        """Enqueues the empty kernel with this plan's launch geometry."""
+        _check(self._lib.moe_finalize_rmsnorm_launch_floor(self._h, _stream_handle(stream)),
+               "moe_finalize_rmsnorm_launch_floor")
 
     def get_status(self, stream=None) -> int:
         st = ctypes.c_int(0)

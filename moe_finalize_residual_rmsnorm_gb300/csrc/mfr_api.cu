@@ -69,6 +69,7 @@ int auto_cluster(int64_t T, int chunks, int sm_count) {
 }
 
 constexpr int64_t kDecodeMaxTokens = 128;
+constexpr int kMaxStages = 8;
 
 }  // namespace
 
@@ -104,7 +105,7 @@ int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int
     mfr_options o;
     moe_finalize_rmsnorm_default_options(&o);
     if (opt) o = *opt;
-    if (o.force_variant < MFR_VARIANT_AUTO || o.force_variant > MFR_VARIANT_ROWS)
+    if (o.force_variant < MFR_VARIANT_AUTO || o.force_variant > MFR_VARIANT_STREAM)
         return fail(MFR_ERR_INVALID_ARG, "force_variant %d is not available", o.force_variant);
     if (!(o.cluster_size == 0 || o.cluster_size == 1 || o.cluster_size == 2 ||
           o.cluster_size == 4 || o.cluster_size == 8 || o.cluster_size == 16))
@@ -113,10 +114,11 @@ int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) { cudaGetLastError(); return fail_cuda(MFR_ERR_BAD_DEVICE, "cudaGetDevice", e); }
-    int major = 0, minor = 0, sms = 0;
+    int major = 0, minor = 0, sms = 0, smem_optin = 0;
     if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) {
         cudaGetLastError();
         return fail_cuda(MFR_ERR_BAD_DEVICE, "cudaDeviceGetAttribute", e);
     }
@@ -130,38 +132,62 @@ int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int
     l.grid_y = 1;
     int variant = o.force_variant;
     int csize = o.cluster_size;
+    // ring depth the bulk-copy kernel would get on this device
+    const int stage_bytes = mfr::stream_stage_bytes(k);
+    const int ring_budget = smem_optin - 1024;                // static shared memory and slack
+    int stages = 0;
+    while (stages < kMaxStages && mfr::stream_smem_bytes(k, stages + 1) <= ring_budget) ++stages;
     if (variant == MFR_VARIANT_AUTO) {
-        if (csize == 0) csize = (T <= kDecodeMaxTokens) ? auto_cluster(T, chunks, sms) : 1;
-        variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
+        if (T <= kDecodeMaxTokens) {
+            if (csize == 0) csize = auto_cluster(T, chunks, sms);
+            variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
+        } else {
+            variant = stages >= 2 ? MFR_VARIANT_STREAM : MFR_VARIANT_ROWS;
+        }
     } else if (variant == MFR_VARIANT_CLUSTER) {
         if (csize == 0) csize = auto_cluster(T, chunks, sms);
         if (csize < 2) csize = 2;
-    } else {
-        csize = 1;
     }
-    if (chunks % csize != 0)
-        return fail(MFR_ERR_UNSUPPORTED_SHAPE, "cluster of %d CTAs needs H/8 divisible by it (H=%lld)",
-                    csize, (long long)H);
-    const int cta_chunks = chunks / csize;
+    if (variant != MFR_VARIANT_CLUSTER) csize = 1;
     l.variant = variant;
-    l.cluster = csize;
-    l.cpt = pick_cpt(cta_chunks);
-    if (l.cpt == 0) return fail(MFR_ERR_UNSUPPORTED_SHAPE, "H=%lld too wide", (long long)H);
-    l.block = round_up((cta_chunks + l.cpt - 1) / l.cpt, 32);
-    l.grid_x = static_cast<int>(T > 0 ? T * csize : csize);
-    l.smem_bytes = 0;
 
-    if ((e = mfr::rows_prepare(l)) != cudaSuccess) {
-        cudaGetLastError();
-        return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
-    }
-    if (csize > 1) {
-        int nclusters = 0;
-        e = mfr::rows_max_active_clusters(l, &nclusters);
-        if (e != cudaSuccess || nclusters < 1) {
+    if (variant == MFR_VARIANT_STREAM) {
+        if (stages < 2)
+            return fail(MFR_ERR_UNSUPPORTED_SHAPE, "k=%d leaves room for fewer than 2 stages of %d bytes",
+                        k, stage_bytes);
+        l.cluster = 1;
+        l.cpt = 1;
+        l.block = mfr::stream_threads();
+        l.stages = stages;
+        l.smem_bytes = mfr::stream_smem_bytes(k, stages);
+        l.grid_x = static_cast<int>(T < sms ? (T > 0 ? T : 1) : sms);
+        if ((e = mfr::stream_prepare(static_cast<int>(H), l.smem_bytes)) != cudaSuccess) {
             cudaGetLastError();
-            return fail(MFR_ERR_UNSUPPORTED_SHAPE, "a cluster of %d CTAs x %d threads cannot be resident",
-                        csize, l.block);
+            return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
+        }
+    } else {
+        if (chunks % csize != 0)
+            return fail(MFR_ERR_UNSUPPORTED_SHAPE, "cluster of %d CTAs needs H/8 divisible by it (H=%lld)",
+                        csize, (long long)H);
+        const int cta_chunks = chunks / csize;
+        l.cluster = csize;
+        l.cpt = pick_cpt(cta_chunks);
+        if (l.cpt == 0) return fail(MFR_ERR_UNSUPPORTED_SHAPE, "H=%lld too wide", (long long)H);
+        l.block = round_up((cta_chunks + l.cpt - 1) / l.cpt, 32);
+        l.grid_x = static_cast<int>(T > 0 ? T * csize : csize);
+        l.smem_bytes = 0;
+        if ((e = mfr::rows_prepare(l)) != cudaSuccess) {
+            cudaGetLastError();
+            return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
+        }
+        if (csize > 1) {
+            int nclusters = 0;
+            e = mfr::rows_max_active_clusters(l, &nclusters);
+            if (e != cudaSuccess || nclusters < 1) {
+                cudaGetLastError();
+                return fail(MFR_ERR_UNSUPPORTED_SHAPE, "a cluster of %d CTAs x %d threads cannot be resident",
+                            csize, l.block);
+            }
         }
     }
 
@@ -249,7 +275,8 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int3
     p.eps = eps;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    e = mfr::rows_launch(p, plan->launch, s);
+    e = plan->launch.variant == MFR_VARIANT_STREAM ? mfr::stream_launch(p, plan->launch, s)
+                                                   : mfr::rows_launch(p, plan->launch, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail_cuda(MFR_ERR_LAUNCH, "kernel launch", e);
@@ -258,6 +285,8 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int3
         int st = 0;
         const int rc = moe_finalize_rmsnorm_get_status(plan, stream, &st);
         if (rc != MFR_OK) return rc;
+        if (st & MFR_STATUS_TIMEOUT)
+            return fail(MFR_ERR_CUDA, "an on-chip wait timed out; the outputs are not valid");
         if (st & MFR_STATUS_BAD_INDEX)
             return fail(MFR_ERR_BAD_INDEX, "a permuted_row_of entry was outside [0, %lld)", (long long)R);
     }
@@ -277,6 +306,18 @@ int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_s
         return fail_cuda(MFR_ERR_CUDA, "reading the status word", e);
     }
     *device_status = h;
+    return MFR_OK;
+}
+
+int moe_finalize_rmsnorm_launch_floor(mfr_plan_t plan, void* stream) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    if (plan->T == 0) return MFR_OK;
+    const cudaError_t e = mfr::floor_launch(plan->d_status, plan->launch, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_LAUNCH, "floor kernel launch", e);
+    }
     return MFR_OK;
 }
 

@@ -34,6 +34,7 @@ struct Launch {
     int smem_bytes;   // dynamic shared memory
     int cpt;          // 16-byte chunks per thread per row
     int pdl;          // programmatic stream serialization
+    int stages;       // MFR_VARIANT_STREAM: shared-memory ring depth
 };
 
 constexpr int kMaxK = 16;         // slots per token
@@ -45,5 +46,14 @@ bool rows_supported_cpt(int cpt);
 cudaError_t rows_prepare(const Launch& l);   // per-kernel attributes (cluster > 8)
 cudaError_t rows_max_active_clusters(const Launch& l, int* n);
 cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s);
+// An empty kernel with the plan's launch geometry (for the launch floor).
+cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s);
+
+// mfr_stream.cu: persistent CTAs fed by bulk copies into a shared-memory ring.
+int stream_threads();
+int stream_stage_bytes(int k);
+int stream_smem_bytes(int k, int nstages);
+cudaError_t stream_prepare(int H, int smem_bytes);
+cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s);
 
 }  // namespace mfr

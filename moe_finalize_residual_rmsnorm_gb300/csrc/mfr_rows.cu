@@ -187,7 +187,7 @@ RowsKernel rows_kernel_for(int cpt) {
     switch (cpt) {
         case 1: return rows_kernel<1, 8>;
         case 2: return rows_kernel<2, 8>;
-        case 4: return rows_kernel<4, 4>;
+        case 4: return rows_kernel<4, 2>;
         default: return nullptr;
     }
 }
@@ -216,7 +216,31 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attrs, const Laun
     cfg.numAttrs = static_cast<unsigned>(n);
 }
 
+// Same launch protocol as the real kernels and nothing else: the PDL wait and
+// trigger.  Timing it with a plan's exact geometry gives the launch floor.
+__global__ void floor_kernel(int* status) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (status == nullptr && threadIdx.x == 0x7FFFFFFF) *status = 0;  // never taken; keeps the argument
+}
+
 }  // namespace
+
+cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s) {
+    if (l.smem_bytes > 0) {
+        cudaError_t e = cudaFuncSetAttribute(floor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             l.smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    if (l.cluster > 8) {
+        cudaError_t e = cudaFuncSetAttribute(floor_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attrs[2];
+    fill_config(cfg, attrs, l, s);
+    return cudaLaunchKernelEx(&cfg, floor_kernel, status);
+}
 
 bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt) != nullptr; }
 

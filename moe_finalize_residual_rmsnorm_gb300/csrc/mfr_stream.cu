@@ -1,0 +1,341 @@
+// Persistent bulk-copy kernel (MFR_VARIANT_STREAM).
+//
+// One CTA per SM walks a static list of tokens (t = blockIdx.x, += gridDim.x).
+// A producer warp stages, for each token and each column tile of width
+// CB = 8 * NT, the k gathered expert-row segments and the residual segment
+// into a ring of shared-memory stages with bulk asynchronous copies
+// (cp.async.bulk, completion counted in bytes on an mbarrier).  NT consumer
+// threads each own one 16-byte chunk of every tile: they wait for a stage,
+// accumulate acc = fma(w_j, e_j, acc) in slot order, add the residual, write
+// residual_out, release the stage, and keep x in registers; after the last
+// tile of a token they reduce the sum of squares (warp butterfly, then warps
+// in index order) and write the bf16 output.
+//
+// The ring keeps several tiles in flight per SM at all times, so the gather
+// never drains between tokens (the register-gather kernel stalls on each
+// token's index load and block barrier).  Operation and citations are those
+// of the register-gather kernel: FlashInfer PR 5319 analysis section 1 (FP32
+// FMA in slot order, bf16 at the end), PR 4730 analysis section 2 (sum,
+// residual, RMSNorm fused), PR 5319 analysis section 2 (dependent launch).
+//
+// Every wait on an mbarrier is bounded: past ~2 s the thread records
+// MFR_STATUS_TIMEOUT and stops; before the CTA exits, the producer waits
+// (again bounded) for the copies it issued, so no copy is left in flight.
+#include "mfr_device.cuh"
+#include "mfr_internal.h"
+
+namespace mfr {
+namespace {
+
+constexpr int kStreamNT = 256;                 // consumer threads (8 warps)
+constexpr int kStreamThreads = kStreamNT + 32; // + one producer warp
+constexpr int kStreamCB = kStreamNT * 8;       // columns per tile
+constexpr int kHeaderBytes = 128;              // per stage: weights + slot mask
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+struct StageHeader {
+    float w[kMaxK];
+    uint32_t mask;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test_parity(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Waits for the phase with the given parity to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_test_parity(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test_parity(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory; completion is counted on bar.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// MAXTILES: upper bound on ceil(H / CB) for this instantiation.
+template <int MAXTILES>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+stream_kernel(const Params p, const int nstages, const int stage_bytes)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    // layout: [nstages full barriers][nstages empty barriers][pad to 128]
+    //         then nstages x { header (128 B) | k row segments (CB*2 each) | residual (CB*4) }
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    unsigned char* stages = smem + ((2 * nstages * 8 + 127) / 128) * 128;
+    __shared__ float s_warp[kStreamNT / 32];
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x;
+    const int H = p.H;
+    const int k = p.k;
+    const int ntiles = (H + kStreamCB - 1) / kStreamCB;
+    const int row_bytes = kStreamCB * 2;   // one slot's segment
+    const int res_off = kHeaderBytes + k * row_bytes;
+
+    if (tid == 0) {
+        for (int s = 0; s < nstages; ++s) {
+            mbar_init(smem_u32(&bars[s]), 1);                      // full: producer arrive + tx bytes
+            mbar_init(smem_u32(&bars[nstages + s]), kStreamNT / 32); // empty: one arrive per consumer warp
+        }
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (tid >= kStreamNT) {
+        // ================= producer warp (one elected lane) =================
+        if (tid != kStreamNT) return;
+        int64_t fill = 0;            // stages issued so far
+        int s = 0;                   // stage of the next fill
+        uint32_t phase = 0;          // how many times the ring wrapped, mod 2
+        bool waited = false;
+        int64_t t = blockIdx.x;
+        // prefetch the slot indices and weights of the first token
+        int32_t nrow[kMaxK];
+        float nw[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            nrow[j] = (j < k && t < p.T) ? p.permuted_row_of[t * k + j] : -1;
+            nw[j] = (j < k && t < p.T) ? p.topk_weights[t * k + j] : 0.f;
+        }
+        bool ok = true;
+        for (; t < p.T && ok; t += gridDim.x) {
+            int32_t row[kMaxK];
+            float w[kMaxK];
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) { row[j] = nrow[j]; w[j] = nw[j]; }
+            const int64_t tn = t + gridDim.x;   // prefetch the next token's slots
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j) {
+                nrow[j] = (j < k && tn < p.T) ? p.permuted_row_of[tn * k + j] : -1;
+                nw[j] = (j < k && tn < p.T) ? p.topk_weights[tn * k + j] : 0.f;
+            }
+            uint32_t mask = 0;
+#pragma unroll
+            for (int j = 0; j < kMaxK; ++j)
+                if (j < k && row[j] >= 0 && static_cast<int64_t>(row[j]) < p.R) mask |= 1u << j;
+            if (mask != (1u << k) - 1u)
+                atomicOr(p.status, MFR_STATUS_BAD_INDEX);
+            if (!waited) {
+                pdl_wait();          // expert_out and residual_in come from the previous kernel
+                waited = true;
+            }
+            for (int b = 0; b < ntiles; ++b) {
+                // the consumers released the previous fill of this stage
+                if (fill >= nstages && !mbar_wait(smem_u32(&bars[nstages + s]), phase ^ 1u)) {
+                    atomicOr(p.status, MFR_STATUS_TIMEOUT);
+                    s_abort = 1;
+                    ok = false;
+                    break;
+                }
+                unsigned char* st = stages + static_cast<size_t>(s) * stage_bytes;
+                StageHeader* hd = reinterpret_cast<StageHeader*>(st);
+#pragma unroll
+                for (int j = 0; j < kMaxK; ++j) hd->w[j] = w[j];
+                hd->mask = mask;
+                const int c0 = b * kStreamCB;
+                const int cb = min(kStreamCB, H - c0);
+                const uint32_t bar = smem_u32(&bars[s]);
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask) * cb * 2 + cb * 4));
+#pragma unroll
+                for (int j = 0; j < kMaxK; ++j)
+                    if (mask & (1u << j))
+                        bulk_g2s(smem_u32(st + kHeaderBytes + j * row_bytes),
+                                 p.expert_out + static_cast<int64_t>(row[j]) * H + c0,
+                                 static_cast<uint32_t>(cb * 2), bar);
+                bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
+                ++fill;
+                if (++s == nstages) { s = 0; phase ^= 1u; }
+            }
+        }
+        pdl_launch_dependents();
+        // drain: every copy this thread issued has landed before the CTA exits
+        for (int64_t f = (fill > nstages ? fill - nstages : 0); f < fill; ++f) {
+            const int sf = static_cast<int>(f % nstages);
+            if (!mbar_wait(smem_u32(&bars[sf]), static_cast<uint32_t>(f / nstages) & 1u)) {
+                atomicOr(p.status, MFR_STATUS_TIMEOUT);
+                break;
+            }
+        }
+        return;
+    }
+
+    // ===================== consumer threads =====================
+    const int warp = tid >> 5;
+    uint32_t g[MAXTILES][4];
+#pragma unroll
+    for (int b = 0; b < MAXTILES; ++b) {
+        const int col = b * kStreamCB + tid * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (b < ntiles && col < H) v = *reinterpret_cast<const uint4*>(p.gamma + col);
+        g[b][0] = v.x; g[b][1] = v.y; g[b][2] = v.z; g[b][3] = v.w;
+    }
+    pdl_wait();
+
+    int s = 0;
+    uint32_t phase = 0;
+    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
+        float x[MAXTILES][8];
+        float ss = 0.f;
+        bool ok = true;
+#pragma unroll
+        for (int b = 0; b < MAXTILES; ++b) {
+            if (b >= ntiles) break;
+            const uint32_t bar = smem_u32(&bars[s]);
+            const uint32_t ebar = smem_u32(&bars[nstages + s]);
+            const unsigned char* st = stages + static_cast<size_t>(s) * stage_bytes;
+            // one decision per warp, so every lane reaches the same __syncwarp
+            const bool landed = __all_sync(0xFFFFFFFFu, mbar_wait(bar, phase));
+            if (++s == nstages) { s = 0; phase ^= 1u; }
+            if (!landed) {
+                atomicOr(p.status, MFR_STATUS_TIMEOUT);
+                ok = false;
+                break;
+            }
+            const StageHeader* hd = reinterpret_cast<const StageHeader*>(st);
+            const uint32_t mask = hd->mask;
+            const int c0 = b * kStreamCB;
+            const int cb = min(kStreamCB, H - c0);
+            const bool mine = tid * 8 < cb;
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+            if (mine) {
+#pragma unroll
+                for (int j = 0; j < kMaxK; ++j) {
+                    if (j < k && (mask & (1u << j))) {
+                        const float wj = hd->w[j];
+                        const uint4 v = *reinterpret_cast<const uint4*>(st + kHeaderBytes + j * row_bytes + tid * 16);
+                        float e[8];
+                        unpack8(v, e);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc[q] = __fmaf_rn(wj, e[q], acc[q]);
+                    }
+                }
+                const float4 r0 = *reinterpret_cast<const float4*>(st + res_off + tid * 32);
+                const float4 r1 = *reinterpret_cast<const float4*>(st + res_off + tid * 32 + 16);
+                x[b][0] = r0.x + acc[0]; x[b][1] = r0.y + acc[1];
+                x[b][2] = r0.z + acc[2]; x[b][3] = r0.w + acc[3];
+                x[b][4] = r1.x + acc[4]; x[b][5] = r1.y + acc[5];
+                x[b][6] = r1.z + acc[6]; x[b][7] = r1.w + acc[7];
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) x[b][q] = 0.f;
+            }
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(ebar);   // this warp is done with the stage
+            if (mine) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) ss = __fmaf_rn(x[b][q], x[b][q], ss);
+                float* ro = p.residual_out + t * H + c0 + tid * 8;
+                st_f4(ro, make_float4(x[b][0], x[b][1], x[b][2], x[b][3]));
+                st_f4(ro + 4, make_float4(x[b][4], x[b][5], x[b][6], x[b][7]));
+            }
+        }
+        ss = warp_allreduce_sum(ss);
+        if ((tid & 31) == 0) s_warp[warp] = ss;
+        // consumer-only barrier that also ORs "stop" over every consumer
+        // thread, so all of them take the same decision
+        const uint32_t stop_in = (!ok || s_abort != 0) ? 1u : 0u;
+        uint32_t stop;
+        asm volatile("{\n\t.reg .pred pin, pout;\n\t"
+                     "setp.ne.u32 pin, %1, 0;\n\t"
+                     "bar.red.or.pred pout, 1, %2, pin;\n\t"
+                     "selp.u32 %0, 1, 0, pout;\n\t}"
+                     : "=r"(stop) : "r"(stop_in), "r"(kStreamNT) : "memory");
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kStreamNT / 32; ++w) tot += s_warp[w];
+        asm volatile("bar.sync 1, %0;" :: "r"(kStreamNT) : "memory");  // s_warp reusable
+        if (stop) break;
+        const float inv = rsqrtf(tot / static_cast<float>(H) + p.eps);
+#pragma unroll
+        for (int b = 0; b < MAXTILES; ++b) {
+            if (b >= ntiles) break;
+            const int col = b * kStreamCB + tid * 8;
+            if (col < H) {
+                uint4 o;
+                o.x = pack_bf16x2(x[b][0] * inv * bf16_lo(g[b][0]), x[b][1] * inv * bf16_hi(g[b][0]));
+                o.y = pack_bf16x2(x[b][2] * inv * bf16_lo(g[b][1]), x[b][3] * inv * bf16_hi(g[b][1]));
+                o.z = pack_bf16x2(x[b][4] * inv * bf16_lo(g[b][2]), x[b][5] * inv * bf16_hi(g[b][2]));
+                o.w = pack_bf16x2(x[b][6] * inv * bf16_lo(g[b][3]), x[b][7] * inv * bf16_hi(g[b][3]));
+                st_u4(p.out + t * H + col, o);
+            }
+        }
+    }
+}
+
+using StreamKernel = void (*)(const Params, const int, const int);
+
+StreamKernel stream_kernel_for(int H) {
+    const int tiles = (H + kStreamCB - 1) / kStreamCB;
+    if (tiles <= 2) return stream_kernel<2>;
+    if (tiles <= 4) return stream_kernel<4>;
+    if (tiles <= 8) return stream_kernel<8>;
+    return nullptr;
+}
+
+}  // namespace
+
+int stream_threads() { return kStreamThreads; }
+
+int stream_stage_bytes(int k) { return kHeaderBytes + k * kStreamCB * 2 + kStreamCB * 4; }
+
+int stream_smem_bytes(int k, int nstages) {
+    return ((2 * nstages * 8 + 127) / 128) * 128 + nstages * stream_stage_bytes(k);
+}
+
+cudaError_t stream_prepare(int H, int smem_bytes) {
+    StreamKernel kf = stream_kernel_for(H);
+    if (!kf) return cudaErrorInvalidValue;
+    return cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s) {
+    StreamKernel kf = stream_kernel_for(p.H);
+    if (!kf) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(l.grid_x), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(l.block), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(l.smem_bytes);
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[1];
+    int n = 0;
+    if (l.pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = static_cast<unsigned>(n);
+    return cudaLaunchKernelEx(&cfg, kf, p, l.stages, stream_stage_bytes(p.k));
+}
+
+}  // namespace mfr

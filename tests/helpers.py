@@ -44,9 +44,10 @@ def assert_residual_close(got: np.ndarray, want: np.ndarray, what="residual_out"
     got = np.asarray(got, dtype=np.float32)
     want = np.asarray(want, dtype=np.float32)
     both_nan = np.isnan(got) & np.isnan(want)
-    err = np.abs(got.astype(np.float64) - want.astype(np.float64))
-    tol = np.maximum(RES_REL * np.abs(want.astype(np.float64)), RES_ABS)
-    bad = ~both_nan & ~(err <= tol) & ~(got == want)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(got.astype(np.float64) - want.astype(np.float64))
+        tol = np.maximum(RES_REL * np.abs(want.astype(np.float64)), RES_ABS)
+        bad = ~both_nan & ~(err <= tol) & ~(got == want)
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance; first at {tuple(i)}: "

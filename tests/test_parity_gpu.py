@@ -91,7 +91,8 @@ def test_tiny_ref_auto_plan_is_bit_exact_on_the_residual():
     assert np.mean(got_out != want_out) < 0.02
 
 
-@pytest.mark.parametrize("variant,cluster", [(mfr.VARIANT_ROWS, 0), (mfr.VARIANT_CLUSTER, 2),
+@pytest.mark.parametrize("variant,cluster", [(mfr.VARIANT_ROWS, 0), (mfr.VARIANT_STREAM, 0),
+                                             (mfr.VARIANT_CLUSTER, 2),
                                              (mfr.VARIANT_CLUSTER, 4), (mfr.VARIANT_CLUSTER, 8),
                                              (mfr.VARIANT_CLUSTER, 16)])
 @pytest.mark.parametrize("pdl", [True, False])
@@ -115,13 +116,16 @@ def test_shapes_with_ragged_tails(H, k):
     T = 5
     inp = inputs_for(T, H, k, R=T * k + 3, seed=H + k)
     compare_full(inp)
+    compare_full(inp, dict(variant=mfr.VARIANT_ROWS))
+    compare_full(inp, dict(variant=mfr.VARIANT_STREAM))
     if H % 64 == 0 and H >= 1024:
         compare_full(inp, dict(variant=mfr.VARIANT_CLUSTER, cluster_size=8))
 
 
 def test_in_place_residual():
     inp = W.make_inputs(W.decode(16), "cuda")
-    for kw in (dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=4)):
+    for kw in (dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=4),
+               dict(variant=mfr.VARIANT_STREAM)):
         compare_full(inp, kw, in_place=True)
 
 
@@ -134,8 +138,37 @@ def test_out_of_range_indices_add_nothing_and_raise_the_status_bit():
     idx[5, 3] = 2**31 - 1
     idx[4, 4] = -(2**31)
     inp["permuted_row_of"] = idx
-    for kw in (dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=2)):
+    for kw in (dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=2),
+               dict(variant=mfr.VARIANT_STREAM)):
         compare_full(inp, kw)
+
+
+@pytest.mark.parametrize("T", [129, 151, 152, 153, 304, 1000, 2049])
+@pytest.mark.parametrize("H", [4096, 8192, 1032])
+def test_stream_token_counts_around_the_sm_count(T, H):
+    """The persistent kernel's static token schedule: fewer, equal and more
+    tokens than CTAs, ragged last round, ragged last column tile."""
+    inp = inputs_for(T, H, 8, seed=T + H)
+    _, _, _, _, plan = compare_full(inp, dict(variant=mfr.VARIANT_STREAM))
+    assert plan.info()["variant"] == mfr.VARIANT_STREAM
+
+
+def test_variants_agree_bitwise_on_the_residual():
+    inp = W.make_inputs(W.PREFILL, "cuda", T=300)
+    results = [run_gpu(inp, dict(variant=v, cluster_size=c))
+               for v, c in ((mfr.VARIANT_ROWS, 0), (mfr.VARIANT_STREAM, 0), (mfr.VARIANT_CLUSTER, 4))]
+    for r in results[1:]:
+        assert np.array_equal(r[0].view(np.uint32), results[0][0].view(np.uint32))
+        assert_out_close(r[1], results[0][1])
+
+
+def test_launch_floor_runs_with_every_geometry():
+    for kw in (dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_STREAM),
+               dict(variant=mfr.VARIANT_CLUSTER, cluster_size=16)):
+        plan = mfr.Plan(64, 4096, 8, 512, **kw)
+        plan.launch_floor()
+        torch.cuda.synchronize()
+        assert plan.get_status() == 0
 
 
 def test_debug_checks_turn_a_bad_index_into_an_error():
@@ -188,10 +221,11 @@ def test_zero_tokens_is_a_no_op():
     del z
 
 
-def test_repeated_runs_are_bitwise_identical():
+@pytest.mark.parametrize("variant", [mfr.VARIANT_ROWS, mfr.VARIANT_STREAM])
+def test_repeated_runs_are_bitwise_identical(variant):
     inp = W.make_inputs(W.PREFILL, "cuda", T=1000)
-    a = run_gpu(inp)
-    b = run_gpu(inp)
+    a = run_gpu(inp, dict(variant=variant))
+    b = run_gpu(inp, dict(variant=variant))
     assert np.array_equal(a[0].view(np.uint32), b[0].view(np.uint32))
     assert np.array_equal(a[1], b[1])
 
