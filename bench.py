@@ -45,8 +45,13 @@ import workloads as W  # noqa: E402
 METRIC = "effective HBM GB/s (% of GB300 peak) and µs/call vs tokens T, H=4096/8192, k=8"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["moe_finalize_residual_rmsnorm_gb300/csrc/mfr_rows.cu",
-                  "moe_finalize_residual_rmsnorm_gb300/csrc/mfr_device.cuh"]
+KERNEL_SOURCES = {
+    "stream": ["moe_finalize_residual_rmsnorm_gb300/csrc/mfr_stream.cu",
+               "moe_finalize_residual_rmsnorm_gb300/csrc/mfr_device.cuh"],
+    "rows": ["moe_finalize_residual_rmsnorm_gb300/csrc/mfr_rows.cu",
+             "moe_finalize_residual_rmsnorm_gb300/csrc/mfr_device.cuh"],
+}
+KERNEL_SOURCES["cluster"] = KERNEL_SOURCES["rows"]
 
 
 def parse_args(argv=None):
@@ -62,6 +67,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--variant", default="auto", choices=["auto", "rows", "stream", "cluster"])
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T of the workload (small cases for profiling)")
     return ap.parse_args(argv)
 
 
@@ -178,9 +185,9 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(variant: str):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[variant]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -196,7 +203,7 @@ def recorded_traffic(workload: str, variant: str):
     except (OSError, ValueError):
         return None
     e = d.get(workload, {})
-    if e.get("kernel_hash") != kernel_source_hash() or e.get("variant") != variant:
+    if e.get("variant") != variant or e.get("kernel_hash") != kernel_source_hash(variant):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -275,6 +282,8 @@ def run_ours(args):
     device = torch.device("cuda", local)
     dist = init_dist(world, "nccl")
     wl = W.by_name(args.workload).with_(seed=W.by_name(args.workload).seed + rank)
+    if args.tokens:
+        wl = wl.with_(T=args.tokens)
     T, H, k, R = wl.T, wl.H, wl.k, wl.R
     nbytes = W.algorithmic_bytes(T, H, k)
 
@@ -340,7 +349,7 @@ def run_ours(args):
                    "tokens_per_gpu": T, "hidden": H, "top_k": k, "experts": wl.E,
                    "bytes_per_call": nbytes, "variant": info["variant_name"], "grid": info["grid_x"],
                    "block": info["block"], "cluster": info["cluster"], "pdl": not args.no_pdl,
-                   "l2": "inputs larger than L2 (1.75 GB/call) and 2 alternating input sets",
+                   "l2": f"inputs larger than L2 ({nbytes / 1e9:.2f} GB/call) and 2 alternating input sets",
                    "parallelism": f"replicas x{world} (independent token batches)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
