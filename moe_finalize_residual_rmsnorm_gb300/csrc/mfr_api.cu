@@ -161,7 +161,9 @@ int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int
         l.stages = stages;
         l.smem_bytes = mfr::stream_smem_bytes(k, stages);
         l.grid_x = static_cast<int>(T < sms ? (T > 0 ? T : 1) : sms);
-        if ((e = mfr::stream_prepare(static_cast<int>(H), l.smem_bytes)) != cudaSuccess) {
+        // the attribute is per kernel, shared by every plan: always the device
+        // maximum, so a plan with a deeper ring never loses its setting
+        if ((e = mfr::stream_prepare(static_cast<int>(H), ring_budget)) != cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }

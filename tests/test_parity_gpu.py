@@ -42,14 +42,15 @@ def check_guards(buf, fill):
         "a kernel wrote outside its output"
 
 
-def run_gpu(inp, plan_kw=None, in_place=False, residual=None):
+def run_gpu(inp, plan_kw=None, in_place=False, residual=None, plan=None):
     """Runs one call through the binding (C ABI) with guarded outputs.
     Returns host copies (residual_out f32, out bf16 bits) and the plan."""
     e, idx, w, g = inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], inp["gamma"]
     res = inp["residual"] if residual is None else residual
     T, k = idx.shape
     R, H = e.shape
-    plan = mfr.Plan(T, H, k, R, **(plan_kw or {}))
+    if plan is None:
+        plan = mfr.Plan(T, H, k, R, **(plan_kw or {}))
     ob, out = guarded((T, H), torch.bfloat16, -7.0)
     if in_place:
         rb, rout = guarded((T, H), torch.float32, -3.0)
@@ -65,9 +66,9 @@ def run_gpu(inp, plan_kw=None, in_place=False, residual=None):
     return f32(rout), bf16_bits(out), plan
 
 
-def compare_full(inp, plan_kw=None, in_place=False):
+def compare_full(inp, plan_kw=None, in_place=False, plan=None):
     want_res, want_out, bad = oracle_on(inp)
-    got_res, got_out, plan = run_gpu(inp, plan_kw, in_place)
+    got_res, got_out, plan = run_gpu(inp, plan_kw, in_place, plan=plan)
     assert_residual_close(got_res, want_res)
     assert_out_close(got_out, want_out)
     status = plan.get_status()
@@ -160,6 +161,19 @@ def test_variants_agree_bitwise_on_the_residual():
     for r in results[1:]:
         assert np.array_equal(r[0].view(np.uint32), results[0][0].view(np.uint32))
         assert_out_close(r[1], results[0][1])
+
+
+def test_plans_with_different_rings_coexist():
+    """A k=16 plan (3 stages) keeps working after a k=8 plan (5 stages) of the
+    same kernel was made: the shared-memory attribute is per kernel."""
+    a_inp = inputs_for(300, 4096, 16, seed=11)
+    b_inp = inputs_for(300, 4096, 8, seed=12)
+    a_plan = mfr.Plan(300, 4096, 16, 300 * 16, variant=mfr.VARIANT_STREAM)
+    b_plan = mfr.Plan(300, 4096, 8, 300 * 8, variant=mfr.VARIANT_STREAM)
+    assert a_plan.info()["smem_bytes"] > b_plan.info()["smem_bytes"]
+    compare_full(a_inp, plan=a_plan)
+    compare_full(b_inp, plan=b_plan)
+    compare_full(a_inp, plan=a_plan)
 
 
 def test_launch_floor_runs_with_every_geometry():
