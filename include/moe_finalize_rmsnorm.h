@@ -158,6 +158,42 @@ int moe_finalize_rmsnorm_plan_info(mfr_plan_t plan, mfr_plan_info* info);
  * sure no run of this plan is still in flight. */
 void moe_finalize_rmsnorm_destroy(mfr_plan_t plan);
 
+/* ---- allocation-free entry point ---------------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory: engines that own all device memory
+ * through their own pool and forbid allocations outside it, and hosts where
+ * cudaMalloc's implicit synchronisation is not allowed on the request path.
+ * moe_finalize_rmsnorm_plan allocates a device status word with cudaMalloc;
+ * this call needs no plan and allocates nothing (no cudaMalloc, no cudaFree,
+ * no allocating library routine).
+ *
+ * Scratch: the kernel's status word lives in a file-scope __device__ array
+ * of MFR_NOALLOC_SLOTS ints (256 bytes), which every GPU that loads the
+ * library keeps until the process exits.  `slot` picks the word this call
+ * uses; a slot outside [0, MFR_NOALLOC_SLOTS) is rejected with
+ * MFR_ERR_INVALID_ARG ("beyond the scratch").  The array keeps the last
+ * call's contents, so every call first clears its word (an asynchronous
+ * memset on `stream`).  Calls that use the same slot and overlap on the GPU
+ * (different streams, or graph branches) race on that word: give concurrent
+ * streams different slots.
+ *
+ * Set-up: the first call on a device (made with that device current) looks up
+ * the array's device address with cudaGetSymbolAddress, queries the device
+ * and sets the kernel's shared-memory attribute; make that first call before
+ * any stream capture.  Later calls on the device reuse it.
+ *
+ * Arguments and layouts are those of moe_finalize_rmsnorm_run, with T, H, k
+ * and R passed directly.  It always launches the persistent bulk-copy kernel
+ * (MFR_VARIANT_STREAM geometry, PDL on).  If host_status is not NULL the call
+ * waits for `stream` and stores the slot's MFR_STATUS_* bits there; if it is
+ * NULL the call is fully asynchronous and the status is not reported. */
+#define MFR_NOALLOC_SLOTS 64
+int moe_finalize_rmsnorm_run_noalloc(int64_t T, int64_t H, int k, int64_t R,
+                                     const void* expert_out, const int32_t* permuted_row_of,
+                                     const float* topk_weights, const float* residual_in,
+                                     float* residual_out, const void* gamma, float eps, void* out,
+                                     int slot, int* host_status, void* stream);
+
 /* Static text for a return code. */
 const char* moe_finalize_rmsnorm_strerror(int code);
 

@@ -69,6 +69,8 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_get_status": (_I, [_VP, _VP, ctypes.POINTER(_I)]),
     "moe_finalize_rmsnorm_plan_info": (_I, [_VP, ctypes.POINTER(PlanInfo)]),
     "moe_finalize_rmsnorm_launch_floor": (_I, [_VP, _VP]),
+    "moe_finalize_rmsnorm_run_noalloc": (_I, [_I64, _I64, _I, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _I,
+                                               ctypes.POINTER(_I), _VP]),
     "moe_finalize_rmsnorm_destroy": (None, [_VP]),
     "moe_finalize_rmsnorm_strerror": (ctypes.c_char_p, [_I]),
     "moe_finalize_rmsnorm_last_error": (ctypes.c_char_p, []),
@@ -220,6 +222,27 @@ class Plan:
 
     def __exit__(self, *exc):
         self.close()
+
+
+NOALLOC_SLOTS = 64
+
+
+def run_noalloc(expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, eps: float, out,
+                *, slot: int = 0, report_status: bool = False, stream=None):
+    """Allocation-free call (C: moe_finalize_rmsnorm_run_noalloc): no plan, no
+    device allocation; the status word is slot `slot` of the library's static
+    scratch.  Returns the status bits when report_status (the call then waits
+    for the stream), else None."""
+    lib = load_library()
+    T, k = permuted_row_of.shape
+    R, H = expert_out.shape
+    st = ctypes.c_int(0)
+    code = lib.moe_finalize_rmsnorm_run_noalloc(
+        T, H, k, R, _ptr(expert_out), _ptr(permuted_row_of), _ptr(topk_weights), _ptr(residual_in),
+        _ptr(residual_out), _ptr(gamma), ctypes.c_float(eps), _ptr(out), int(slot),
+        ctypes.byref(st) if report_status else None, _stream_handle(stream))
+    _check(code, "moe_finalize_rmsnorm_run_noalloc")
+    return st.value if report_status else None
 
 
 def moe_finalize_residual_rmsnorm(expert_out, permuted_row_of, topk_weights, residual, gamma, eps: float,

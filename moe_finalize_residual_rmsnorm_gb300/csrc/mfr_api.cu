@@ -73,6 +73,13 @@ constexpr int kMaxStages = 8;
 
 }  // namespace
 
+void mfr::set_last_error(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+}
+
 extern "C" {
 
 int moe_finalize_rmsnorm_supports(int64_t H, int k) {

@@ -41,6 +41,9 @@ constexpr int kMaxK = 16;         // slots per token
 constexpr int kMaxH = 16384;      // hidden size
 constexpr int kRowsMaxThreads = 512;
 
+// Sets the calling thread's moe_finalize_rmsnorm_last_error() text.
+void set_last_error(const char* fmt, ...);
+
 // mfr_rows.cu: one CTA (or one cluster of CTAs) per token.
 bool rows_supported_cpt(int cpt);
 cudaError_t rows_prepare(const Launch& l);   // per-kernel attributes (cluster > 8)
