@@ -141,6 +141,24 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan,
                              float* residual_out, const void* gamma, float eps,
                              void* out, void* stream);
 
+/* ---- plain finalize (no residual, no norm) ------------------------------
+ * out[t, h] = bf16( sum_j fma(w[t,j], E[idx[t,j], h], .) ), the FP32 weighted
+ * sum in slot order rounded once to bf16: the finalize kernel of
+ * "FlashInfer MoE 성능 최적화: CuTe DSL을 활용한 Deterministic Finalize
+ * 개선기" (flashinfer PR 5319 analysis), section 1.
+ * moe_finalize_plan takes the same arguments and options as
+ * moe_finalize_rmsnorm_plan (cluster_size then splits the columns of a token
+ * over that many CTAs, without a cluster; nothing is reduced).
+ * moe_finalize_run: expert_out bf16 [R, H] and out bf16 [T, H] 16-byte
+ * aligned, permuted_row_of / topk_weights [T, k] 4-byte aligned, out overlaps
+ * no input; bad indices behave as in moe_finalize_rmsnorm_run.  Each plan
+ * kind works only with its own run function (MFR_ERR_INVALID_ARG otherwise);
+ * _get_status, _plan_info, _launch_floor and _destroy take either kind. */
+int moe_finalize_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                      const mfr_options* opt);
+int moe_finalize_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
+                     const float* topk_weights, void* out, void* stream);
+
 /* Waits for `stream`, reads the plan's status word into *device_status
  * (MFR_STATUS_* bits) and clears it.  Returns MFR_OK or a CUDA error code. */
 int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_status);

@@ -19,7 +19,7 @@ from typing import Optional
 from .build import LIBRARY, build as _build_library
 
 __all__ = [
-    "LIBRARY", "MFRError", "Plan", "PlanInfo", "Options", "build", "load_library", "supports",
+    "LIBRARY", "MFRError", "Plan", "FinalizePlan", "PlanInfo", "Options", "build", "load_library", "supports",
     "moe_finalize_residual_rmsnorm", "finalize_residual_rmsnorm_host", "exported_symbols",
     "VARIANT_AUTO", "VARIANT_CLUSTER", "VARIANT_ROWS", "VARIANT_STREAM", "STATUS_BAD_INDEX",
     "ERROR_CODES",
@@ -69,6 +69,8 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_get_status": (_I, [_VP, _VP, ctypes.POINTER(_I)]),
     "moe_finalize_rmsnorm_plan_info": (_I, [_VP, ctypes.POINTER(PlanInfo)]),
     "moe_finalize_rmsnorm_launch_floor": (_I, [_VP, _VP]),
+    "moe_finalize_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
+    "moe_finalize_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_finalize_rmsnorm_run_noalloc": (_I, [_I64, _I64, _I, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _I,
                                                ctypes.POINTER(_I), _VP]),
     "moe_finalize_rmsnorm_destroy": (None, [_VP]),
@@ -136,6 +138,8 @@ class Plan:
     """A plan for T tokens, hidden size H, top-k k and R rows of expert_out on
     the current CUDA device (C: moe_finalize_rmsnorm_plan)."""
 
+    _PLAN_FN = "moe_finalize_rmsnorm_plan"
+
     def __init__(self, T: int, H: int, k: int, R: Optional[int] = None, *, enable_pdl: bool = True,
                  variant: int = VARIANT_AUTO, cluster_size: int = 0, debug_checks: bool = False):
         lib = load_library()
@@ -144,8 +148,8 @@ class Plan:
         self.R = int(T) * int(k) if R is None else int(R)
         opt = Options(int(bool(enable_pdl)), int(variant), int(cluster_size), int(bool(debug_checks)))
         h = ctypes.c_void_p()
-        _check(lib.moe_finalize_rmsnorm_plan(ctypes.byref(h), self.T, self.H, self.k, self.R,
-                                             ctypes.byref(opt)), "moe_finalize_rmsnorm_plan")
+        _check(getattr(lib, self._PLAN_FN)(ctypes.byref(h), self.T, self.H, self.k, self.R,
+                                           ctypes.byref(opt)), self._PLAN_FN)
         self._h = h
 
     @property
@@ -222,6 +226,26 @@ class Plan:
 
     def __exit__(self, *exc):
         self.close()
+
+
+class FinalizePlan(Plan):
+    """Plain finalize, out = bf16(FP32 weighted sum), no residual and no norm
+    (C: moe_finalize_plan / moe_finalize_run)."""
+
+    _PLAN_FN = "moe_finalize_plan"
+
+    def run(self, expert_out, permuted_row_of, topk_weights, out, stream=None, *, validate: bool = True):
+        if validate:
+            import torch
+            for name, t, dt, shape in [("expert_out", expert_out, torch.bfloat16, (self.R, self.H)),
+                                       ("permuted_row_of", permuted_row_of, torch.int32, (self.T, self.k)),
+                                       ("topk_weights", topk_weights, torch.float32, (self.T, self.k)),
+                                       ("out", out, torch.bfloat16, (self.T, self.H))]:
+                if t.dtype != dt or tuple(t.shape) != shape or not t.is_cuda or not t.is_contiguous():
+                    raise ValueError(f"{name}: expected contiguous CUDA {dt} {shape}")
+        code = self._lib.moe_finalize_run(self._h, _ptr(expert_out), _ptr(permuted_row_of), _ptr(topk_weights),
+                                          _ptr(out), _stream_handle(stream))
+        _check(code, "moe_finalize_run")
 
 
 NOALLOC_SLOTS = 64

@@ -21,6 +21,7 @@ struct mfr_plan_s {
     mfr_options opt;
     mfr::Launch launch;
     int* d_status;
+    bool fused;        // made by moe_finalize_rmsnorm_plan (true) or moe_finalize_plan (false)
 };
 
 namespace {
@@ -94,8 +95,13 @@ void moe_finalize_rmsnorm_default_options(mfr_options* opt) {
     opt->debug_checks = 0;
 }
 
-int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
-                              const mfr_options* opt) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the fused plan (residual + RMSNorm) and the plain-finalize plan.
+int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mfr_options* opt,
+              bool fused) {
     g_last_error[0] = '\0';
     if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
     *plan = nullptr;
@@ -137,13 +143,14 @@ int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int
     mfr::Launch l{};
     l.pdl = o.enable_pdl ? 1 : 0;
     l.grid_y = 1;
+    l.fused = fused ? 1 : 0;
     int variant = o.force_variant;
     int csize = o.cluster_size;
     // ring depth the bulk-copy kernel would get on this device
-    const int stage_bytes = mfr::stream_stage_bytes(k);
+    const int stage_bytes = mfr::stream_stage_bytes(k, fused);
     const int ring_budget = smem_optin - 1024;                // static shared memory and slack
     int stages = 0;
-    while (stages < kMaxStages && mfr::stream_smem_bytes(k, stages + 1) <= ring_budget) ++stages;
+    while (stages < kMaxStages && mfr::stream_smem_bytes(k, stages + 1, fused) <= ring_budget) ++stages;
     if (variant == MFR_VARIANT_AUTO) {
         if (T <= kDecodeMaxTokens) {
             if (csize == 0) csize = auto_cluster(T, chunks, sms);
@@ -166,11 +173,11 @@ int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int
         l.cpt = 1;
         l.block = mfr::stream_threads();
         l.stages = stages;
-        l.smem_bytes = mfr::stream_smem_bytes(k, stages);
+        l.smem_bytes = mfr::stream_smem_bytes(k, stages, fused);
         l.grid_x = static_cast<int>(T < sms ? (T > 0 ? T : 1) : sms);
         // the attribute is per kernel, shared by every plan: always the device
         // maximum, so a plan with a deeper ring never loses its setting
-        if ((e = mfr::stream_prepare(static_cast<int>(H), ring_budget)) != cudaSuccess) {
+        if ((e = mfr::stream_prepare(static_cast<int>(H), fused, ring_budget)) != cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }
@@ -189,7 +196,7 @@ int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }
-        if (csize > 1) {
+        if (csize > 1 && fused) {
             int nclusters = 0;
             e = mfr::rows_max_active_clusters(l, &nclusters);
             if (e != cudaSuccess || nclusters < 1) {
@@ -224,7 +231,76 @@ int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int
     p->opt = o;
     p->launch = l;
     p->d_status = status;
+    p->fused = fused;
     *plan = p;
+    return MFR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                              const mfr_options* opt) {
+    return make_plan(plan, T, H, k, R, opt, true);
+}
+
+int moe_finalize_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mfr_options* opt) {
+    return make_plan(plan, T, H, k, R, opt, false);
+}
+
+int moe_finalize_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
+                     const float* topk_weights, void* out, void* stream) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    if (plan->fused) return fail(MFR_ERR_INVALID_ARG, "this plan was made by moe_finalize_rmsnorm_plan");
+    const int64_t T = plan->T, H = plan->H, R = plan->R;
+    const int k = plan->k;
+    if (T == 0) return MFR_OK;
+    if (!permuted_row_of || !topk_weights || !out || (R > 0 && !expert_out))
+        return fail(MFR_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned(expert_out, 16) || !aligned(out, 16))
+        return fail(MFR_ERR_MISALIGNED, "expert_out and out must be 16-byte aligned");
+    if (!aligned(permuted_row_of, 4) || !aligned(topk_weights, 4))
+        return fail(MFR_ERR_MISALIGNED, "permuted_row_of and topk_weights must be 4-byte aligned");
+    const size_t n_out = static_cast<size_t>(T * H) * 2;
+    const size_t n_e = static_cast<size_t>(R * H) * 2;
+    const size_t n_tk = static_cast<size_t>(T * k) * 4;
+    if (overlaps(out, n_out, expert_out, n_e) || overlaps(out, n_out, permuted_row_of, n_tk) ||
+        overlaps(out, n_out, topk_weights, n_tk))
+        return fail(MFR_ERR_INVALID_ARG, "out overlaps an input");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { cudaGetLastError(); return fail_cuda(MFR_ERR_CUDA, "cudaGetDevice", e); }
+    if (dev != plan->device)
+        return fail(MFR_ERR_INVALID_ARG, "current device %d is not the plan's device %d", dev, plan->device);
+
+    mfr::Params p{};
+    p.expert_out = static_cast<const uint16_t*>(expert_out);
+    p.permuted_row_of = permuted_row_of;
+    p.topk_weights = topk_weights;
+    p.out = static_cast<uint16_t*>(out);
+    p.status = plan->d_status;
+    p.T = T;
+    p.R = R;
+    p.H = static_cast<int>(H);
+    p.k = k;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = plan->launch.variant == MFR_VARIANT_STREAM ? mfr::stream_launch(p, plan->launch, s)
+                                                   : mfr::rows_launch(p, plan->launch, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_LAUNCH, "kernel launch", e);
+    }
+    if (plan->opt.debug_checks) {
+        int st = 0;
+        const int rc = moe_finalize_rmsnorm_get_status(plan, stream, &st);
+        if (rc != MFR_OK) return rc;
+        if (st & MFR_STATUS_TIMEOUT)
+            return fail(MFR_ERR_CUDA, "an on-chip wait timed out; the outputs are not valid");
+        if (st & MFR_STATUS_BAD_INDEX)
+            return fail(MFR_ERR_BAD_INDEX, "a permuted_row_of entry was outside [0, %lld)", (long long)R);
+    }
     return MFR_OK;
 }
 
@@ -233,6 +309,7 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int3
                              const void* gamma, float eps, void* out, void* stream) {
     g_last_error[0] = '\0';
     if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    if (!plan->fused) return fail(MFR_ERR_INVALID_ARG, "this plan was made by moe_finalize_plan");
     const int64_t T = plan->T, H = plan->H, R = plan->R;
     const int k = plan->k;
     if (T == 0) return MFR_OK;

@@ -23,6 +23,13 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Ask L2 to fetch `bytes` (multiple of 16, 16-byte aligned address) ahead of
+// use.  A prefetch has no effect on what later loads return, so it may run
+// before pdl_wait(): loads after the wait still see the producer's writes.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(ptr), "r"(bytes) : "memory");
+}
+
 // ---- loads and stores --------------------------------------------------------
 // 16 bytes of read-only, read-once data: skip L1 and ask L2 for a 256-byte
 // prefetch (the rows are long and contiguous).  volatile keeps it after

@@ -35,6 +35,7 @@ struct Launch {
     int cpt;          // 16-byte chunks per thread per row
     int pdl;          // programmatic stream serialization
     int stages;       // MFR_VARIANT_STREAM: shared-memory ring depth
+    int fused;        // 1: residual + RMSNorm; 0: plain finalize (out = bf16(sum))
 };
 
 constexpr int kMaxK = 16;         // slots per token
@@ -54,9 +55,9 @@ cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s);
 
 // mfr_stream.cu: persistent CTAs fed by bulk copies into a shared-memory ring.
 int stream_threads();
-int stream_stage_bytes(int k);
-int stream_smem_bytes(int k, int nstages);
-cudaError_t stream_prepare(int H, int smem_bytes);
+int stream_stage_bytes(int k, bool fused);
+int stream_smem_bytes(int k, int nstages, bool fused);
+cudaError_t stream_prepare(int H, bool fused, int smem_bytes);
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s);
 
 }  // namespace mfr

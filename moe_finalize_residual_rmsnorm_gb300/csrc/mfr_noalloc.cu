@@ -73,7 +73,7 @@ int setup_device(int dev, DeviceSetup* out) {
         // one attribute per kernel instantiation (by column tiles per token),
         // set to the device maximum exactly as the planned path sets it
         for (int h : {4096, 8192, 16384}) {
-            if (mfr::stream_prepare(h, budget) != cudaSuccess) {
+            if (mfr::stream_prepare(h, true, budget) != cudaSuccess) {
                 cudaGetLastError();
                 return MFR_ERR_CUDA;
             }
@@ -133,7 +133,7 @@ extern "C" int moe_finalize_rmsnorm_run_noalloc(
         return mfr::set_last_error("set-up of device %d failed (needs sm_103)", dev), rc;
 
     int stages = 0;
-    while (stages < kMaxStagesNoAlloc && mfr::stream_smem_bytes(k, stages + 1) <= ds.ring_budget) ++stages;
+    while (stages < kMaxStagesNoAlloc && mfr::stream_smem_bytes(k, stages + 1, true) <= ds.ring_budget) ++stages;
     if (stages < 2) return mfr::set_last_error("k=%d leaves no room for 2 ring stages", k), MFR_ERR_UNSUPPORTED_SHAPE;
 
     mfr::Launch l{};
@@ -144,8 +144,9 @@ extern "C" int moe_finalize_rmsnorm_run_noalloc(
     l.cluster = 1;
     l.cpt = 1;
     l.stages = stages;
-    l.smem_bytes = mfr::stream_smem_bytes(k, stages);
+    l.smem_bytes = mfr::stream_smem_bytes(k, stages, true);
     l.pdl = 1;
+    l.fused = 1;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* status = ds.status + slot;

@@ -4,7 +4,9 @@
 // (MFR_VARIANT_CLUSTER).
 //
 // Per token t, for the columns this CTA owns:
-//   prologue  : slot indices and weights of t, gamma        (before the PDL wait)
+//   trigger   : let the next kernel in the stream start its prologue
+//   prologue  : slot indices and weights of t, gamma; ask L2 to prefetch the
+//               CTA's row and residual segments             (before the PDL wait)
 //   wait      : the producer of expert_out / residual_in has finished
 //   gather    : k rows of expert_out, 16 bytes per load, all loads of a slot
 //               group issued before any is used
@@ -16,6 +18,9 @@
 //               warps in index order, then (cluster) CTAs in rank order
 //               through DSMEM (PR 4730 analysis, section 2: cluster exchange)
 //   normalise : y = (x * rsqrt(ss / H + eps)) * gamma, rounded to bf16
+// With FUSED = false the kernel is the plain finalize of the PR 5319 page:
+// out = bf16(acc), no residual, no norm; the C CTAs of a token then split
+// the columns without a cluster (nothing to reduce).
 // Every reduction order is fixed by (H, k, launch geometry), so a plan gives
 // bitwise-identical results on every run.
 #include <cooperative_groups.h>
@@ -25,11 +30,19 @@
 
 namespace cg = cooperative_groups;
 
+#ifndef MFR_ROWS_EARLY_TRIGGER
+#define MFR_ROWS_EARLY_TRIGGER 1
+#endif
+#ifndef MFR_ROWS_PREFETCH_L2
+#define MFR_ROWS_PREFETCH_L2 1
+#endif
+
 namespace mfr {
 namespace {
 
-// CPT: 16-byte column chunks per thread per row; SG: slots gathered together.
-template <int CPT, int SG>
+// CPT: 16-byte column chunks per thread per row; SG: slots gathered together;
+// FUSED: residual + RMSNorm (true) or plain finalize (false).
+template <int CPT, int SG, bool FUSED>
 __global__ void __launch_bounds__(kRowsMaxThreads)
 rows_kernel(const Params p, const int csize)
 {
@@ -39,13 +52,17 @@ rows_kernel(const Params p, const int csize)
     const int rank = static_cast<int>(blockIdx.x - t * csize);
     const int nck = (p.H >> 3) / csize;        // chunks of this CTA
     const int64_t col0 = static_cast<int64_t>(rank) * nck * 8;
+    const bool cluster = FUSED && csize > 1;
 
     __shared__ int s_row[kMaxK];
     __shared__ float s_w[kMaxK];
     __shared__ float s_warp[kRowsMaxThreads / 32];
     __shared__ float s_cta[16];
 
-    if (csize > 1)
+#if MFR_ROWS_EARLY_TRIGGER
+    pdl_launch_dependents();   // the next kernel may start its prologue now
+#endif
+    if (cluster)
         cg::this_cluster().barrier_arrive();   // peers write s_cta only after all CTAs started
 
     // ---- prologue: inputs that the producing kernel does not write --------
@@ -61,20 +78,30 @@ rows_kernel(const Params p, const int csize)
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
         const int c = tid + i * nthreads;
-        g[i] = (c < nck) ? *reinterpret_cast<const uint4*>(p.gamma + col0 + c * 8)
-                         : make_uint4(0, 0, 0, 0);
+        g[i] = (FUSED && c < nck) ? *reinterpret_cast<const uint4*>(p.gamma + col0 + c * 8)
+                                  : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
+
+#if MFR_ROWS_PREFETCH_L2
+    // warm L2 with this CTA's row segments and residual segment while the
+    // previous kernel finishes
+    if (tid < p.k && s_row[tid] >= 0)
+        prefetch_l2_bulk(p.expert_out + static_cast<int64_t>(s_row[tid]) * p.H + col0,
+                         static_cast<uint32_t>(nck) * 16u);
+    else if (FUSED && tid == kMaxK)
+        prefetch_l2_bulk(p.residual_in + t * p.H + col0, static_cast<uint32_t>(nck) * 32u);
+#endif
 
     pdl_wait();
 
     // ---- residual row and the k expert rows ---------------------------------
-    const float* res_in = p.residual_in + t * p.H + col0;
     float res[CPT][8];
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
         const int c = tid + i * nthreads;
-        if (c < nck) {
+        if (FUSED && c < nck) {
+            const float* res_in = p.residual_in + t * p.H + col0;
             const float4 a = ld_once_f4(res_in + c * 8);
             const float4 b = ld_once_f4(res_in + c * 8 + 4);
             res[i][0] = a.x; res[i][1] = a.y; res[i][2] = a.z; res[i][3] = a.w;
@@ -120,6 +147,27 @@ rows_kernel(const Params p, const int csize)
         }
     }
 
+    if constexpr (!FUSED) {
+        // ---- plain finalize: out = bf16(acc) --------------------------------
+        uint16_t* out = p.out + t * p.H + col0;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int c = tid + i * nthreads;
+            if (c < nck) {
+                uint4 o;
+                o.x = pack_bf16x2(acc[i][0], acc[i][1]);
+                o.y = pack_bf16x2(acc[i][2], acc[i][3]);
+                o.z = pack_bf16x2(acc[i][4], acc[i][5]);
+                o.w = pack_bf16x2(acc[i][6], acc[i][7]);
+                st_u4(out + c * 8, o);
+            }
+        }
+#if !MFR_ROWS_EARLY_TRIGGER
+        pdl_launch_dependents();
+#endif
+        return;
+    }
+
     // ---- x = residual + acc; write the residual; sum of squares ------------
     float* res_out = p.residual_out + t * p.H + col0;
     float ss = 0.f;
@@ -146,21 +194,23 @@ rows_kernel(const Params p, const int csize)
     for (int w = 0; w < nwarps; ++w)
         tot += s_warp[w];
 
-    if (csize > 1) {
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.barrier_wait();                      // all CTAs have started
+    if (cluster) {
+        cg::cluster_group cl = cg::this_cluster();
+        cl.barrier_wait();                           // all CTAs have started
         if (tid < csize) {
-            float* dst = cluster.map_shared_rank(&s_cta[rank], tid);
+            float* dst = cl.map_shared_rank(&s_cta[rank], tid);
             *dst = tot;
         }
-        cluster.barrier_arrive();
-        cluster.barrier_wait();                      // every partial has landed
+        cl.barrier_arrive();
+        cl.barrier_wait();                           // every partial has landed
         tot = 0.f;
         for (int r = 0; r < csize; ++r)
             tot += s_cta[r];
     }
 
+#if !MFR_ROWS_EARLY_TRIGGER
     pdl_launch_dependents();
+#endif
 
     // ---- y = (x * inv) * gamma -> bf16 ----------------------------------------
     const float inv = rsqrtf(tot / static_cast<float>(p.H) + p.eps);
@@ -183,11 +233,11 @@ rows_kernel(const Params p, const int csize)
 
 using RowsKernel = void (*)(const Params, const int);
 
-RowsKernel rows_kernel_for(int cpt) {
+RowsKernel rows_kernel_for(int cpt, bool fused) {
     switch (cpt) {
-        case 1: return rows_kernel<1, 8>;
-        case 2: return rows_kernel<2, 8>;
-        case 4: return rows_kernel<4, 2>;
+        case 1: return fused ? rows_kernel<1, 8, true> : rows_kernel<1, 8, false>;
+        case 2: return fused ? rows_kernel<2, 8, true> : rows_kernel<2, 8, false>;
+        case 4: return fused ? rows_kernel<4, 2, true> : rows_kernel<4, 2, false>;
         default: return nullptr;
     }
 }
@@ -200,7 +250,7 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attrs, const Laun
     cfg.dynamicSmemBytes = static_cast<size_t>(l.smem_bytes);
     cfg.stream = s;
     int n = 0;
-    if (l.cluster > 1) {
+    if (l.cluster > 1 && l.fused) {
         attrs[n].id = cudaLaunchAttributeClusterDimension;
         attrs[n].val.clusterDim.x = static_cast<unsigned>(l.cluster);
         attrs[n].val.clusterDim.y = 1;
@@ -216,11 +266,16 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attrs, const Laun
     cfg.numAttrs = static_cast<unsigned>(n);
 }
 
-// Same launch protocol as the real kernels and nothing else: the PDL wait and
-// trigger.  Timing it with a plan's exact geometry gives the launch floor.
+// Same launch protocol as the real kernels and nothing else: the PDL trigger
+// and wait.  Timing it with a plan's exact geometry gives the launch floor.
 __global__ void floor_kernel(int* status) {
+#if MFR_ROWS_EARLY_TRIGGER
+    pdl_launch_dependents();
+    pdl_wait();
+#else
     pdl_wait();
     pdl_launch_dependents();
+#endif
     if (status == nullptr && threadIdx.x == 0x7FFFFFFF) *status = 0;  // never taken; keeps the argument
 }
 
@@ -242,18 +297,18 @@ cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, floor_kernel, status);
 }
 
-bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt) != nullptr; }
+bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt, true) != nullptr; }
 
 cudaError_t rows_prepare(const Launch& l) {
-    RowsKernel k = rows_kernel_for(l.cpt);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0);
     if (!k) return cudaErrorInvalidValue;
-    if (l.cluster > 8)
+    if (l.cluster > 8 && l.fused)
         return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return cudaSuccess;
 }
 
 cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
-    RowsKernel k = rows_kernel_for(l.cpt);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];
@@ -262,7 +317,7 @@ cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
 }
 
 cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    RowsKernel k = rows_kernel_for(l.cpt);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];

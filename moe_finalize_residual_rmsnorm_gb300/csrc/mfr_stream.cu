@@ -11,6 +11,9 @@
 // tile of a token they reduce the sum of squares (warp butterfly, then warps
 // in index order) and write the bf16 output.
 //
+// With FUSED = false it is the plain finalize of the PR 5319 page: no
+// residual in the stages, out = bf16(acc) written tile by tile, no norm.
+//
 // The ring keeps several tiles in flight per SM at all times, so the gather
 // never drains between tokens (the register-gather kernel stalls on each
 // token's index load and block barrier).  Operation and citations are those
@@ -23,6 +26,10 @@
 // (again bounded) for the copies it issued, so no copy is left in flight.
 #include "mfr_device.cuh"
 #include "mfr_internal.h"
+
+#ifndef MFR_STREAM_EARLY_TRIGGER
+#define MFR_STREAM_EARLY_TRIGGER 1
+#endif
 
 namespace mfr {
 namespace {
@@ -79,8 +86,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
-// MAXTILES: upper bound on ceil(H / CB) for this instantiation.
-template <int MAXTILES>
+// MAXTILES: upper bound on ceil(H / CB) for this instantiation;
+// FUSED: residual + RMSNorm (true) or plain finalize (false).
+template <int MAXTILES, bool FUSED>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 stream_kernel(const Params p, const int nstages, const int stage_bytes)
 {
@@ -112,6 +120,9 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     if (tid >= kStreamNT) {
         // ================= producer warp (one elected lane) =================
         if (tid != kStreamNT) return;
+#if MFR_STREAM_EARLY_TRIGGER
+        pdl_launch_dependents();
+#endif
         int64_t fill = 0;            // stages issued so far
         int s = 0;                   // stage of the next fill
         uint32_t phase = 0;          // how many times the ring wrapped, mod 2
@@ -163,19 +174,22 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 const int c0 = b * kStreamCB;
                 const int cb = min(kStreamCB, H - c0);
                 const uint32_t bar = smem_u32(&bars[s]);
-                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask) * cb * 2 + cb * 4));
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask) * cb * 2 + (FUSED ? cb * 4 : 0)));
 #pragma unroll
                 for (int j = 0; j < kMaxK; ++j)
                     if (mask & (1u << j))
                         bulk_g2s(smem_u32(st + kHeaderBytes + j * row_bytes),
                                  p.expert_out + static_cast<int64_t>(row[j]) * H + c0,
                                  static_cast<uint32_t>(cb * 2), bar);
-                bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
+                if (FUSED)
+                    bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
                 ++fill;
                 if (++s == nstages) { s = 0; phase ^= 1u; }
             }
         }
+#if !MFR_STREAM_EARLY_TRIGGER
         pdl_launch_dependents();
+#endif
         // drain: every copy this thread issued has landed before the CTA exits
         for (int64_t f = (fill > nstages ? fill - nstages : 0); f < fill; ++f) {
             const int sf = static_cast<int>(f % nstages);
@@ -194,13 +208,62 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     for (int b = 0; b < MAXTILES; ++b) {
         const int col = b * kStreamCB + tid * 8;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (b < ntiles && col < H) v = *reinterpret_cast<const uint4*>(p.gamma + col);
+        if (FUSED && b < ntiles && col < H) v = *reinterpret_cast<const uint4*>(p.gamma + col);
         g[b][0] = v.x; g[b][1] = v.y; g[b][2] = v.z; g[b][3] = v.w;
     }
     pdl_wait();
 
     int s = 0;
     uint32_t phase = 0;
+    if constexpr (!FUSED) {
+        // ---- plain finalize: every tile goes straight to out ----------------
+        for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
+            bool ok = true;
+            for (int b = 0; b < ntiles; ++b) {
+                const uint32_t bar = smem_u32(&bars[s]);
+                const uint32_t ebar = smem_u32(&bars[nstages + s]);
+                const unsigned char* st = stages + static_cast<size_t>(s) * stage_bytes;
+                const bool landed = __all_sync(0xFFFFFFFFu, mbar_wait(bar, phase));
+                if (++s == nstages) { s = 0; phase ^= 1u; }
+                if (!landed) {
+                    atomicOr(p.status, MFR_STATUS_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                const StageHeader* hd = reinterpret_cast<const StageHeader*>(st);
+                const uint32_t mask = hd->mask;
+                const int c0 = b * kStreamCB;
+                const bool mine = tid * 8 < min(kStreamCB, H - c0);
+                float acc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+                if (mine) {
+#pragma unroll
+                    for (int j = 0; j < kMaxK; ++j) {
+                        if (j < k && (mask & (1u << j))) {
+                            const float wj = hd->w[j];
+                            const uint4 v = *reinterpret_cast<const uint4*>(st + kHeaderBytes + j * row_bytes + tid * 16);
+                            float e[8];
+                            unpack8(v, e);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) acc[q] = __fmaf_rn(wj, e[q], acc[q]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if ((tid & 31) == 0) mbar_arrive(ebar);
+                if (mine) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[0], acc[1]);
+                    o.y = pack_bf16x2(acc[2], acc[3]);
+                    o.z = pack_bf16x2(acc[4], acc[5]);
+                    o.w = pack_bf16x2(acc[6], acc[7]);
+                    st_u4(p.out + t * H + c0 + tid * 8, o);
+                }
+            }
+            if (!ok) break;     // warp-uniform: this warp stops; the others time out on their own
+        }
+    } else {
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
         float x[MAXTILES][8];
         float ss = 0.f;
@@ -290,15 +353,16 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
             }
         }
     }
+    }  // FUSED
 }
 
 using StreamKernel = void (*)(const Params, const int, const int);
 
-StreamKernel stream_kernel_for(int H) {
+StreamKernel stream_kernel_for(int H, bool fused) {
     const int tiles = (H + kStreamCB - 1) / kStreamCB;
-    if (tiles <= 2) return stream_kernel<2>;
-    if (tiles <= 4) return stream_kernel<4>;
-    if (tiles <= 8) return stream_kernel<8>;
+    if (tiles <= 2) return fused ? stream_kernel<2, true> : stream_kernel<2, false>;
+    if (tiles <= 4) return fused ? stream_kernel<4, true> : stream_kernel<4, false>;
+    if (tiles <= 8) return fused ? stream_kernel<8, true> : stream_kernel<8, false>;
     return nullptr;
 }
 
@@ -306,20 +370,22 @@ StreamKernel stream_kernel_for(int H) {
 
 int stream_threads() { return kStreamThreads; }
 
-int stream_stage_bytes(int k) { return kHeaderBytes + k * kStreamCB * 2 + kStreamCB * 4; }
-
-int stream_smem_bytes(int k, int nstages) {
-    return ((2 * nstages * 8 + 127) / 128) * 128 + nstages * stream_stage_bytes(k);
+int stream_stage_bytes(int k, bool fused) {
+    return kHeaderBytes + k * kStreamCB * 2 + (fused ? kStreamCB * 4 : 0);
 }
 
-cudaError_t stream_prepare(int H, int smem_bytes) {
-    StreamKernel kf = stream_kernel_for(H);
+int stream_smem_bytes(int k, int nstages, bool fused) {
+    return ((2 * nstages * 8 + 127) / 128) * 128 + nstages * stream_stage_bytes(k, fused);
+}
+
+cudaError_t stream_prepare(int H, bool fused, int smem_bytes) {
+    StreamKernel kf = stream_kernel_for(H, fused);
     if (!kf) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    StreamKernel kf = stream_kernel_for(p.H);
+    StreamKernel kf = stream_kernel_for(p.H, l.fused != 0);
     if (!kf) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid_x), 1, 1);
@@ -335,7 +401,7 @@ cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s) {
     }
     cfg.attrs = attrs;
     cfg.numAttrs = static_cast<unsigned>(n);
-    return cudaLaunchKernelEx(&cfg, kf, p, l.stages, stream_stage_bytes(p.k));
+    return cudaLaunchKernelEx(&cfg, kf, p, l.stages, stream_stage_bytes(p.k, l.fused != 0));
 }
 
 }  // namespace mfr

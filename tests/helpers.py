@@ -69,3 +69,9 @@ def oracle_on(inputs: dict, tokens=None, residual=None):
     return oracle.finalize_residual_rmsnorm(
         bf16_bits(inputs["expert_out"]), inputs["permuted_row_of"].cpu().numpy(),
         f32(inputs["topk_weights"]), res, bf16_bits(inputs["gamma"]), inputs["eps"], tokens=tokens)
+
+
+def oracle_finalize_only(inputs: dict, tokens=None):
+    """The oracle's plain finalize on host copies: (out_bits, bad_slots)."""
+    return oracle.finalize_only(bf16_bits(inputs["expert_out"]), inputs["permuted_row_of"].cpu().numpy(),
+                                f32(inputs["topk_weights"]), tokens=tokens)

@@ -1,0 +1,94 @@
+"""The plain finalize (out = bf16 of the FP32 weighted sum; no residual, no
+norm) against the oracle's finalize: bf16 output within 1 ulp (in practice
+equal: both round the same FP32 value once)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_finalize_residual_rmsnorm_gb300 as mfr
+import workloads as W
+from helpers import assert_out_close, bf16_bits, oracle_finalize_only
+
+pytestmark = pytest.mark.gpu
+GUARD = 256
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    mfr.build()
+    mfr.load_library()
+
+
+def run_finalize(inp, **plan_kw):
+    e, idx, w = inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"]
+    T, k = idx.shape
+    R, H = e.shape
+    plan = mfr.FinalizePlan(T, H, k, R, **plan_kw)
+    buf = torch.full((T * H + 2 * GUARD,), -5.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[GUARD:GUARD + T * H].view(T, H)
+    plan.run(e, idx, w, out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:GUARD] == -5.0) and torch.all(buf[-GUARD:] == -5.0)
+    return bf16_bits(out), plan
+
+
+VARIANTS = [dict(), dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_STREAM),
+            dict(variant=mfr.VARIANT_CLUSTER, cluster_size=4)]
+
+
+@pytest.mark.parametrize("kw", VARIANTS, ids=["auto", "rows", "stream", "split4"])
+@pytest.mark.parametrize("T,H,k", [(1, 4096, 8), (16, 4096, 8), (5, 24, 3), (300, 8192, 8), (7, 4104, 16),
+                                   (153, 1032, 1)])
+def test_finalize_only_matches_oracle(kw, T, H, k):
+    if kw.get("cluster_size") and (H // 8) % kw["cluster_size"]:
+        pytest.skip("column split must divide H/8")
+    wl = W.Workload(f"fin_T{T}_H{H}", T=T, H=H, k=k, E=max(16, 2 * k), seed=T * 7 + H + k, extra_rows=2)
+    inp = W.make_inputs(wl, "cuda")
+    want, bad = oracle_finalize_only(inp)
+    got, plan = run_finalize(inp, **kw)
+    assert bad == 0
+    assert_out_close(got, want)
+    assert np.array_equal(got, want)       # same FP32 value rounded once on both sides
+    assert plan.get_status() == 0
+
+
+def test_finalize_only_bad_indices():
+    inp = W.make_inputs(W.decode(8), "cuda")
+    inp["permuted_row_of"][2, 5] = -1
+    inp["permuted_row_of"][6, 0] = 10**6
+    for kw in VARIANTS:
+        want, bad = oracle_finalize_only(inp)
+        got, plan = run_finalize(inp, **kw)
+        assert bad == 2
+        assert np.array_equal(got, want)
+        assert plan.get_status() & mfr.STATUS_BAD_INDEX
+
+
+def test_plan_kinds_do_not_mix():
+    inp = W.make_inputs(W.decode(2), "cuda")
+    fin = mfr.FinalizePlan(2, 4096, 8)
+    fused = mfr.Plan(2, 4096, 8)
+    out = torch.empty((2, 4096), dtype=torch.bfloat16, device="cuda")
+    rout = torch.empty_like(inp["residual"])
+    with pytest.raises(mfr.MFRError):          # residual + norm run on a finalize plan
+        mfr.Plan.run(fin, inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], inp["residual"], rout,
+                     inp["gamma"], 1e-6, out)
+    with pytest.raises(mfr.MFRError):
+        mfr.FinalizePlan.run(fused, inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], out)
+
+
+@pytest.mark.parametrize("wl", [W.PREFILL, W.STRESS], ids=lambda w: w.name)
+def test_finalize_only_full_size_sampled(wl):
+    inp = W.make_inputs(wl, "cuda")
+    T = wl.T
+    plan = mfr.FinalizePlan(T, wl.H, wl.k, wl.R)
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    plan.run(inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], out)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=40, replace=False)]))
+    want, bad = oracle_finalize_only(inp, tokens=tokens)
+    assert bad == 0
+    assert np.array_equal(bf16_bits(out)[tokens], want)
