@@ -60,16 +60,20 @@ int pick_cpt(int chunks) {
     return 0;
 }
 
-// Cluster size for few tokens: enough CTAs to cover the SMs, a power of two
-// dividing the chunk count, and at least one warp of chunks per CTA.
-int auto_cluster(int64_t T, int chunks, int sm_count) {
-    int c = 1;
-    while (c < 8 && T * c < sm_count) c *= 2;
+// Cluster size for the split-H variant: the largest power of two <= 8 that
+// divides the chunk count and leaves at least one warp of chunks per CTA.
+int auto_cluster(int chunks) {
+    int c = 8;
     while (c > 1 && (chunks % c != 0 || chunks / c < 32)) c /= 2;
     return c;
 }
 
-constexpr int64_t kDecodeMaxTokens = 128;
+// Variant choice by the number of elements T*H of a call (measured on GB300
+// with cold inputs): up to 2^18 a cluster of 8 CTAs per token is fastest (few
+// tokens, latency bound); up to 3*2^20 one CTA per token; beyond that the
+// persistent ring kernel, whose per-SM pipeline needs enough tokens per SM.
+constexpr int64_t kClusterMaxElems = int64_t(1) << 18;
+constexpr int64_t kRowsMaxElems = int64_t(3) << 20;
 constexpr int kMaxStages = 8;
 
 }  // namespace
@@ -152,14 +156,17 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     int stages = 0;
     while (stages < kMaxStages && mfr::stream_smem_bytes(k, stages + 1, fused) <= ring_budget) ++stages;
     if (variant == MFR_VARIANT_AUTO) {
-        if (T <= kDecodeMaxTokens) {
-            if (csize == 0) csize = auto_cluster(T, chunks, sms);
+        const int64_t elems = T * H;
+        if (elems <= kClusterMaxElems) {
+            if (csize == 0) csize = auto_cluster(chunks);
             variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
+        } else if (elems < kRowsMaxElems || stages < 2) {
+            variant = MFR_VARIANT_ROWS;
         } else {
-            variant = stages >= 2 ? MFR_VARIANT_STREAM : MFR_VARIANT_ROWS;
+            variant = MFR_VARIANT_STREAM;
         }
     } else if (variant == MFR_VARIANT_CLUSTER) {
-        if (csize == 0) csize = auto_cluster(T, chunks, sms);
+        if (csize == 0) csize = auto_cluster(chunks);
         if (csize < 2) csize = 2;
     }
     if (variant != MFR_VARIANT_CLUSTER) csize = 1;

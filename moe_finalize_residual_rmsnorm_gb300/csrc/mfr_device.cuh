@@ -31,12 +31,12 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes
 }
 
 // ---- loads and stores --------------------------------------------------------
-// 16 bytes of read-only, read-once data: skip L1 and ask L2 for a 256-byte
-// prefetch (the rows are long and contiguous).  volatile keeps it after
-// pdl_wait().
+// 16 bytes of read-once data, cached in L2 only (.cg): the rows were written
+// by the previous kernel and, for few tokens, prefetched into L2 by the
+// prologue.  volatile keeps it after pdl_wait().
 __device__ __forceinline__ uint4 ld_stream_u4(const void* ptr) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(ptr));
     return v;
@@ -59,6 +59,57 @@ __device__ __forceinline__ void st_f4(float* ptr, float4 v) {
 __device__ __forceinline__ void st_u4(void* ptr, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
                  :: "l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// ---- shared-memory barriers and cluster stores ---------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+// Arrive once and announce `bytes` of asynchronous writes for this phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test_parity(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Waits (bounded, ~2 s at 2 GHz) for the phase with this parity to complete.
+constexpr long long kWaitCycles = 4000000000LL;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_test_parity(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test_parity(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    return remote;
+}
+
+// One-way 4-byte store into a peer CTA's shared memory; its arrival is
+// counted (4 bytes) on the peer's mbarrier.
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t remote, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 :: "r"(remote), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
 }
 
 // ---- bf16 -----------------------------------------------------------------------

@@ -15,8 +15,10 @@
 //   residual  : x = residual_in + acc, written to residual_out
 //               (FlashInfer PR 4730 analysis, section 2: sum, residual, RMSNorm fused)
 //   reduce    : sum of x^2 — per thread in column order, a warp butterfly,
-//               warps in index order, then (cluster) CTAs in rank order
-//               through DSMEM (PR 4730 analysis, section 2: cluster exchange)
+//               warps in index order, then (cluster) CTAs in rank order: each
+//               CTA pushes its partial into every peer's shared memory with
+//               st.async, counted on the peer's mbarrier (PR 4730 analysis,
+//               section 2: cluster exchange through distributed shared memory)
 //   normalise : y = (x * rsqrt(ss / H + eps)) * gamma, rounded to bf16
 // With FUSED = false the kernel is the plain finalize of the PR 5319 page:
 // out = bf16(acc), no residual, no norm; the C CTAs of a token then split
@@ -30,12 +32,6 @@
 
 namespace cg = cooperative_groups;
 
-#ifndef MFR_ROWS_EARLY_TRIGGER
-#define MFR_ROWS_EARLY_TRIGGER 1
-#endif
-#ifndef MFR_ROWS_PREFETCH_L2
-#define MFR_ROWS_PREFETCH_L2 1
-#endif
 
 namespace mfr {
 namespace {
@@ -59,11 +55,20 @@ rows_kernel(const Params p, const int csize)
     __shared__ float s_warp[kRowsMaxThreads / 32];
     __shared__ float s_cta[16];
 
-#if MFR_ROWS_EARLY_TRIGGER
     pdl_launch_dependents();   // the next kernel may start its prologue now
-#endif
-    if (cluster)
-        cg::this_cluster().barrier_arrive();   // peers write s_cta only after all CTAs started
+    // cluster exchange: every CTA will receive csize partial sums (4 bytes
+    // each) on s_bar; peers send only after the cluster barrier below, which
+    // also publishes the barrier's initialisation
+    __shared__ __align__(8) uint64_t s_bar;
+    if (cluster) {
+        if (tid == 0) {
+            mbar_init(smem_addr(&s_bar), 1);
+            mbar_arrive_expect_tx(smem_addr(&s_bar), static_cast<uint32_t>(csize) * 4u);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        cg::this_cluster().barrier_arrive();
+    }
 
     // ---- prologue: inputs that the producing kernel does not write --------
     if (tid < p.k) {
@@ -83,7 +88,6 @@ rows_kernel(const Params p, const int csize)
     }
     __syncthreads();
 
-#if MFR_ROWS_PREFETCH_L2
     // warm L2 with this CTA's row segments and residual segment while the
     // previous kernel finishes
     if (tid < p.k && s_row[tid] >= 0)
@@ -91,7 +95,6 @@ rows_kernel(const Params p, const int csize)
                          static_cast<uint32_t>(nck) * 16u);
     else if (FUSED && tid == kMaxK)
         prefetch_l2_bulk(p.residual_in + t * p.H + col0, static_cast<uint32_t>(nck) * 32u);
-#endif
 
     pdl_wait();
 
@@ -162,9 +165,6 @@ rows_kernel(const Params p, const int csize)
                 st_u4(out + c * 8, o);
             }
         }
-#if !MFR_ROWS_EARLY_TRIGGER
-        pdl_launch_dependents();
-#endif
         return;
     }
 
@@ -195,22 +195,19 @@ rows_kernel(const Params p, const int csize)
         tot += s_warp[w];
 
     if (cluster) {
-        cg::cluster_group cl = cg::this_cluster();
-        cl.barrier_wait();                           // all CTAs have started
-        if (tid < csize) {
-            float* dst = cl.map_shared_rank(&s_cta[rank], tid);
-            *dst = tot;
-        }
-        cl.barrier_arrive();
-        cl.barrier_wait();                           // every partial has landed
+        // one-way delivery of this CTA's partial into slot [rank] of every
+        // peer (itself included); then wait until all csize partials are here.
+        // A CTA leaves only after every write into its shared memory landed.
+        cg::this_cluster().barrier_wait();           // all CTAs started, barriers initialised
+        if (tid < csize)
+            st_async_cluster_f32(cluster_map(smem_addr(&s_cta[rank]), tid), tot,
+                                 cluster_map(smem_addr(&s_bar), tid));
+        if (!mbar_wait(smem_addr(&s_bar), 0))
+            atomicOr(p.status, MFR_STATUS_TIMEOUT);
         tot = 0.f;
         for (int r = 0; r < csize; ++r)
             tot += s_cta[r];
     }
-
-#if !MFR_ROWS_EARLY_TRIGGER
-    pdl_launch_dependents();
-#endif
 
     // ---- y = (x * inv) * gamma -> bf16 ----------------------------------------
     const float inv = rsqrtf(tot / static_cast<float>(p.H) + p.eps);
@@ -269,13 +266,8 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attrs, const Laun
 // Same launch protocol as the real kernels and nothing else: the PDL trigger
 // and wait.  Timing it with a plan's exact geometry gives the launch floor.
 __global__ void floor_kernel(int* status) {
-#if MFR_ROWS_EARLY_TRIGGER
     pdl_launch_dependents();
     pdl_wait();
-#else
-    pdl_wait();
-    pdl_launch_dependents();
-#endif
     if (status == nullptr && threadIdx.x == 0x7FFFFFFF) *status = 0;  // never taken; keeps the argument
 }
 

@@ -27,10 +27,6 @@
 #include "mfr_device.cuh"
 #include "mfr_internal.h"
 
-#ifndef MFR_STREAM_EARLY_TRIGGER
-#define MFR_STREAM_EARLY_TRIGGER 1
-#endif
-
 namespace mfr {
 namespace {
 
@@ -38,46 +34,13 @@ constexpr int kStreamNT = 256;                 // consumer threads (8 warps)
 constexpr int kStreamThreads = kStreamNT + 32; // + one producer warp
 constexpr int kStreamCB = kStreamNT * 8;       // columns per tile
 constexpr int kHeaderBytes = 128;              // per stage: weights + slot mask
-constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 struct StageHeader {
     float w[kMaxK];
     uint32_t mask;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test_parity(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-    return done != 0;
-}
-
-// Waits for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_test_parity(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_test_parity(bar, parity))
-        if (clock64() - t0 > kWaitCycles) return false;
-    return true;
-}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return smem_addr(p); }
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global memory into this CTA's shared memory; completion is counted on bar.
@@ -120,9 +83,7 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     if (tid >= kStreamNT) {
         // ================= producer warp (one elected lane) =================
         if (tid != kStreamNT) return;
-#if MFR_STREAM_EARLY_TRIGGER
-        pdl_launch_dependents();
-#endif
+        pdl_launch_dependents();     // the next kernel may start its prologue now
         int64_t fill = 0;            // stages issued so far
         int s = 0;                   // stage of the next fill
         uint32_t phase = 0;          // how many times the ring wrapped, mod 2
@@ -187,9 +148,6 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 if (++s == nstages) { s = 0; phase ^= 1u; }
             }
         }
-#if !MFR_STREAM_EARLY_TRIGGER
-        pdl_launch_dependents();
-#endif
         // drain: every copy this thread issued has landed before the CTA exits
         for (int64_t f = (fill > nstages ? fill - nstages : 0); f < fill; ++f) {
             const int sf = static_cast<int>(f % nstages);
