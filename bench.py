@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="prefill", choices=sorted(W.all_named()))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sweep", action="store_true", help="also time the decode and wide sweeps")
+    ap.add_argument("--pdl-pairs", action="store_true",
+                    help="also time producer -> finalize pairs with and without dependent launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -362,6 +364,8 @@ def run_ours(args):
     }
     if args.sweep:
         result["sweep"] = run_sweep(mfr, device, args)
+    if args.pdl_pairs:
+        result["pdl_pairs"] = run_pdl_pairs(mfr, device)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(host_copy(sets[0]), wl, args.cpu_seconds)
     if rank == 0:
@@ -457,6 +461,52 @@ def run_sweep(mfr, device, args):
         if plan.get_status(stream) != 0:
             raise RuntimeError(f"the device status word reported an error during {wl.name}")
         del E, idx, w, res, rout, out, base
+        torch.cuda.empty_cache()
+    return rows
+
+
+def run_pdl_pairs(mfr, device):
+    """µs per (producer -> finalize) pair in a CUDA graph, both kernels with
+    and without programmatic dependent launch.  The stand-in producer waits,
+    signals its dependents, stays busy for `busy` cycles (a GEMM's main loop),
+    then writes expert_out; with PDL the finalize's launch and prologue hide
+    behind it.  Input sets rotate so the finalize reads cold residual data."""
+    rows = []
+    for wl in (W.decode(1), W.decode(8), W.decode(128), W.PREFILL):
+        base = W.make_inputs(wl, device)
+        T, H, k, R = wl.T, wl.H, wl.k, wl.R
+        src = base["expert_out"].clone()
+        rout = torch.empty_like(base["residual"])
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        n = 64 if T <= 128 else 8
+        for busy in (0, 10000):
+            rec = {"workload": wl.name, "T": T, "busy_cycles": busy}
+            for pdl in (False, True):
+                plan = mfr.Plan(T, H, k, R, enable_pdl=pdl)
+                stream = torch.cuda.Stream(device)
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(stream):
+                    with torch.cuda.graph(graph, stream=stream):
+                        for _ in range(n):
+                            mfr.bench_producer(src, base["expert_out"], busy_cycles=busy, enable_pdl=pdl,
+                                               stream=stream)
+                            plan.run(base["expert_out"], base["permuted_row_of"], base["topk_weights"],
+                                     base["residual"], rout, base["gamma"], base["eps"], out, stream,
+                                     validate=False)
+                    graph.replay()
+                    stream.synchronize()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(3):
+                        graph.replay()
+                    b.record(stream)
+                    b.synchronize()
+                if plan.get_status(stream) != 0:
+                    raise RuntimeError("status word set during the PDL pairs")
+                rec["us_per_pair_pdl" if pdl else "us_per_pair_serial"] = round(a.elapsed_time(b) * 1e3 / (3 * n), 3)
+            rec["speedup"] = round(rec["us_per_pair_serial"] / rec["us_per_pair_pdl"], 4)
+            rows.append(rec)
+        del base, src, rout, out
         torch.cuda.empty_cache()
     return rows
 

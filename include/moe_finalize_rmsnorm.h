@@ -86,6 +86,12 @@ typedef struct mfr_options {
     int cluster_size;  /* MFR_VARIANT_CLUSTER: CTAs per token (2, 4, 8 or 16); 0 = auto */
     int debug_checks;  /* 1: run() waits for the kernel and returns MFR_ERR_BAD_INDEX
                           when a slot index was out of range (slow; for debugging) */
+    int sentinel_skip; /* 1: a NEGATIVE permuted_row_of entry marks a slot whose expert
+                          is not local (expert parallelism): the slot adds nothing and
+                          is not an error.  Entries >= R still raise
+                          MFR_STATUS_BAD_INDEX.  0: every entry outside [0, R) is an
+                          error.  The skip itself follows the non-local-expert path of
+                          the PR 6544 analysis, section 2.4. */
 } mfr_options;
 
 /* What a plan decided; for tests, benchmarks and logs. */
@@ -175,6 +181,19 @@ int moe_finalize_rmsnorm_plan_info(mfr_plan_t plan, mfr_plan_info* info);
 /* Frees the plan and its status word.  NULL is a no-op.  The caller makes
  * sure no run of this plan is still in flight. */
 void moe_finalize_rmsnorm_destroy(mfr_plan_t plan);
+
+/* ---- benchmarking stand-in for the producer of expert_out ---------------
+ * Enqueues a kernel that follows the protocol the PR 5319 analysis (section
+ * 2) gives the FC2 grouped GEMM: wait for the previous kernel, immediately
+ * signal dependents, stay busy for `busy_cycles` SM cycles (0 to 4e9; the
+ * GEMM's main loop), then copy `rows` x H bf16 values from `src` to
+ * `expert_out` (both device, 16-byte aligned, H % 8 == 0).  enable_pdl = 1
+ * launches it with programmatic stream serialization.  Used to measure how
+ * much of the finalize's prologue hides behind its producer, and to test that
+ * the finalize never reads expert_out before the producer is done.  Not part
+ * of the finalize itself; returns MFR_OK or an MFR_ERR_* code. */
+int moe_finalize_rmsnorm_bench_producer(const void* src, void* expert_out, int64_t rows, int64_t H,
+                                        long long busy_cycles, int enable_pdl, void* stream);
 
 /* ---- allocation-free entry point ---------------------------------------
  * The pages have no counterpart to this entry point; it exists for callers

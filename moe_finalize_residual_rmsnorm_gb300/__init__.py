@@ -45,7 +45,8 @@ class MFRError(RuntimeError):
 
 class Options(ctypes.Structure):
     _fields_ = [("enable_pdl", ctypes.c_int), ("force_variant", ctypes.c_int),
-                ("cluster_size", ctypes.c_int), ("debug_checks", ctypes.c_int)]
+                ("cluster_size", ctypes.c_int), ("debug_checks", ctypes.c_int),
+                ("sentinel_skip", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -69,6 +70,7 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_get_status": (_I, [_VP, _VP, ctypes.POINTER(_I)]),
     "moe_finalize_rmsnorm_plan_info": (_I, [_VP, ctypes.POINTER(PlanInfo)]),
     "moe_finalize_rmsnorm_launch_floor": (_I, [_VP, _VP]),
+    "moe_finalize_rmsnorm_bench_producer": (_I, [_VP, _VP, _I64, _I64, ctypes.c_longlong, _I, _VP]),
     "moe_finalize_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
     "moe_finalize_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_finalize_rmsnorm_run_noalloc": (_I, [_I64, _I64, _I, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _I,
@@ -141,12 +143,14 @@ class Plan:
     _PLAN_FN = "moe_finalize_rmsnorm_plan"
 
     def __init__(self, T: int, H: int, k: int, R: Optional[int] = None, *, enable_pdl: bool = True,
-                 variant: int = VARIANT_AUTO, cluster_size: int = 0, debug_checks: bool = False):
+                 variant: int = VARIANT_AUTO, cluster_size: int = 0, debug_checks: bool = False,
+                 sentinel_skip: bool = False):
         lib = load_library()
         self._lib = lib
         self.T, self.H, self.k = int(T), int(H), int(k)
         self.R = int(T) * int(k) if R is None else int(R)
-        opt = Options(int(bool(enable_pdl)), int(variant), int(cluster_size), int(bool(debug_checks)))
+        opt = Options(int(bool(enable_pdl)), int(variant), int(cluster_size), int(bool(debug_checks)),
+                      int(bool(sentinel_skip)))
         h = ctypes.c_void_p()
         _check(getattr(lib, self._PLAN_FN)(ctypes.byref(h), self.T, self.H, self.k, self.R,
                                            ctypes.byref(opt)), self._PLAN_FN)
@@ -246,6 +250,16 @@ class FinalizePlan(Plan):
         code = self._lib.moe_finalize_run(self._h, _ptr(expert_out), _ptr(permuted_row_of), _ptr(topk_weights),
                                           _ptr(out), _stream_handle(stream))
         _check(code, "moe_finalize_run")
+
+
+def bench_producer(src, expert_out, busy_cycles: int = 0, enable_pdl: bool = True, stream=None) -> None:
+    """Stand-in for the GEMM2 producer (C: moe_finalize_rmsnorm_bench_producer):
+    wait, signal dependents, stay busy, then copy src into expert_out."""
+    lib = load_library()
+    R, H = expert_out.shape
+    _check(lib.moe_finalize_rmsnorm_bench_producer(_ptr(src), _ptr(expert_out), R, H, int(busy_cycles),
+                                                   int(bool(enable_pdl)), _stream_handle(stream)),
+           "moe_finalize_rmsnorm_bench_producer")
 
 
 NOALLOC_SLOTS = 64

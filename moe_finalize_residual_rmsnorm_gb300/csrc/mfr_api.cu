@@ -97,6 +97,7 @@ void moe_finalize_rmsnorm_default_options(mfr_options* opt) {
     opt->force_variant = MFR_VARIANT_AUTO;
     opt->cluster_size = 0;
     opt->debug_checks = 0;
+    opt->sentinel_skip = 0;
 }
 
 }  // extern "C"
@@ -292,6 +293,7 @@ int moe_finalize_run(mfr_plan_t plan, const void* expert_out, const int32_t* per
     p.R = R;
     p.H = static_cast<int>(H);
     p.k = k;
+    p.sentinel = plan->opt.sentinel_skip ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = plan->launch.variant == MFR_VARIANT_STREAM ? mfr::stream_launch(p, plan->launch, s)
                                                    : mfr::rows_launch(p, plan->launch, s);
@@ -366,6 +368,7 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int3
     p.H = static_cast<int>(H);
     p.k = k;
     p.eps = eps;
+    p.sentinel = plan->opt.sentinel_skip ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = plan->launch.variant == MFR_VARIANT_STREAM ? mfr::stream_launch(p, plan->launch, s)

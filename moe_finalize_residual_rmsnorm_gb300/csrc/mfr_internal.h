@@ -22,6 +22,7 @@ struct Params {
     int H;
     int k;
     float eps;
+    int sentinel;                   // 1: a negative index is a skipped non-local slot, not an error
 };
 
 // Launch geometry fixed by the plan.

@@ -74,7 +74,7 @@ rows_kernel(const Params p, const int csize)
     if (tid < p.k) {
         const int32_t r = p.permuted_row_of[t * p.k + tid];
         const bool ok = (r >= 0) && (static_cast<int64_t>(r) < p.R);
-        if (!ok && rank == 0)
+        if (!ok && rank == 0 && !(p.sentinel && r < 0))   // negative = non-local when allowed
             atomicOr(p.status, MFR_STATUS_BAD_INDEX);
         s_row[tid] = ok ? r : -1;
         s_w[tid] = p.topk_weights[t * p.k + tid];

@@ -19,7 +19,8 @@
 // token's index load and block barrier).  Operation and citations are those
 // of the register-gather kernel: FlashInfer PR 5319 analysis section 1 (FP32
 // FMA in slot order, bf16 at the end), PR 4730 analysis section 2 (sum,
-// residual, RMSNorm fused), PR 5319 analysis section 2 (dependent launch).
+// residual, RMSNorm fused), PR 5319 analysis section 2 (dependent launch:
+// slot indices are read before the wait, rows and residual after it).
 //
 // Every wait on an mbarrier is bounded: past ~2 s the thread records
 // MFR_STATUS_TIMEOUT and stops; before the CTA exits, the producer waits
@@ -83,7 +84,10 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     if (tid >= kStreamNT) {
         // ================= producer warp (one elected lane) =================
         if (tid != kStreamNT) return;
-        pdl_launch_dependents();     // the next kernel may start its prologue now
+        // No explicit launch_dependents: every CTA of this persistent grid runs
+        // from start to end, so an early signal would let a dependent grid park
+        // its CTAs on every SM for the whole call (measured: a following
+        // producer slowed the pair by 17 %).  Dependents launch as CTAs exit.
         int64_t fill = 0;            // stages issued so far
         int s = 0;                   // stage of the next fill
         uint32_t phase = 0;          // how many times the ring wrapped, mod 2
@@ -110,10 +114,14 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 nw[j] = (j < k && tn < p.T) ? p.topk_weights[tn * k + j] : 0.f;
             }
             uint32_t mask = 0;
+            bool flag = false;
 #pragma unroll
-            for (int j = 0; j < kMaxK; ++j)
-                if (j < k && row[j] >= 0 && static_cast<int64_t>(row[j]) < p.R) mask |= 1u << j;
-            if (mask != (1u << k) - 1u)
+            for (int j = 0; j < kMaxK; ++j) {
+                if (j >= k) continue;
+                if (row[j] >= 0 && static_cast<int64_t>(row[j]) < p.R) mask |= 1u << j;
+                else if (!(p.sentinel && row[j] < 0)) flag = true;   // negative = non-local when allowed
+            }
+            if (flag)
                 atomicOr(p.status, MFR_STATUS_BAD_INDEX);
             if (!waited) {
                 pdl_wait();          // expert_out and residual_in come from the previous kernel

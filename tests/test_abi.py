@@ -53,9 +53,9 @@ def test_supports_truth_table(lib):
 
 
 def test_default_options(lib):
-    o = mfr.Options(7, 7, 7, 7)
+    o = mfr.Options(7, 7, 7, 7, 7)
     lib.moe_finalize_rmsnorm_default_options(ctypes.byref(o))
-    assert (o.enable_pdl, o.force_variant, o.cluster_size, o.debug_checks) == (1, 0, 0, 0)
+    assert (o.enable_pdl, o.force_variant, o.cluster_size, o.debug_checks, o.sentinel_skip) == (1, 0, 0, 0, 0)
 
 
 def test_strerror_covers_every_code(lib):
@@ -82,9 +82,9 @@ def test_plan_rejects_bad_shapes_before_touching_a_device(lib):
 
 
 def test_plan_rejects_bad_options(lib):
-    rc, _ = _plan(lib, 4, 4096, 8, 32, mfr.Options(1, 9, 0, 0))
+    rc, _ = _plan(lib, 4, 4096, 8, 32, mfr.Options(1, 9, 0, 0, 0))
     assert rc == 1
-    rc, _ = _plan(lib, 4, 4096, 8, 32, mfr.Options(1, 0, 3, 0))
+    rc, _ = _plan(lib, 4, 4096, 8, 32, mfr.Options(1, 0, 3, 0, 0))
     assert rc == 1
 
 

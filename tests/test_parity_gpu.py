@@ -307,3 +307,29 @@ def test_full_size_sampled_tokens(wl):
             torch.cuda.synchronize()
             assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
             assert torch.equal(rout.view(torch.int32), rout2.view(torch.int32))
+
+
+@pytest.mark.parametrize("kw", [dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_STREAM),
+                                dict(variant=mfr.VARIANT_CLUSTER, cluster_size=8)],
+                         ids=["rows", "stream", "cluster8"])
+def test_sentinel_skip_for_non_local_experts(kw):
+    """With sentinel_skip, a negative index is a non-local slot: it adds
+    nothing (as every invalid slot does) and raises no status bit; an index
+    >= R still does."""
+    inp = inputs_for(6, 2048, 8, seed=21)
+    idx = inp["permuted_row_of"].clone()
+    R = inp["expert_out"].shape[0]
+    idx[0, 3] = -1
+    idx[4, 0] = -7
+    inp["permuted_row_of"] = idx
+    want_res, want_out, bad = oracle_on(inp)
+    assert bad == 2
+    got_res, got_out, plan = run_gpu(inp, dict(kw, sentinel_skip=True))
+    assert_residual_close(got_res, want_res)
+    assert_out_close(got_out, want_out)
+    assert plan.get_status() == 0                        # negative entries are not errors
+    _, _, plan = run_gpu(inp, dict(kw, sentinel_skip=False))
+    assert plan.get_status() & mfr.STATUS_BAD_INDEX      # without the option they are
+    idx[2, 2] = R                                         # out of range at the top: always an error
+    got_res, got_out, plan = run_gpu(inp, dict(kw, sentinel_skip=True))
+    assert plan.get_status() & mfr.STATUS_BAD_INDEX
