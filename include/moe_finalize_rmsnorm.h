@@ -165,6 +165,26 @@ int moe_finalize_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
 int moe_finalize_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
                      const float* topk_weights, void* out, void* stream);
 
+/* ---- end to end from host buffers ----------------------------------------
+ * The same call with every tensor in HOST memory.  On `stream`, in order:
+ * one cudaMemcpyAsync per input (expert_out, permuted_row_of, topk_weights,
+ * residual_in, gamma) into the caller's device workspace, the kernel, and one
+ * cudaMemcpyAsync per output (residual_out, out) back to host memory.
+ * Asynchronous: the host outputs are complete when `stream` reaches that
+ * point.  Host buffers should be page-locked (pinned) for the copies to be
+ * asynchronous.  The workspace (device, 256-byte aligned, at least
+ * moe_finalize_rmsnorm_host_workspace_bytes(plan) bytes, owned by the caller)
+ * holds every tensor of one call; calls whose workspaces differ may overlap
+ * on different streams (one call's output copies then run under the next
+ * call's input copies).  Only plans made by moe_finalize_rmsnorm_plan.
+ * host_workspace_bytes returns -1 for a NULL or plain-finalize plan. */
+int64_t moe_finalize_rmsnorm_host_workspace_bytes(mfr_plan_t plan);
+int moe_finalize_rmsnorm_run_host(mfr_plan_t plan, const void* h_expert_out,
+                                  const int32_t* h_permuted_row_of, const float* h_topk_weights,
+                                  const float* h_residual_in, float* h_residual_out,
+                                  const void* h_gamma, float eps, void* h_out,
+                                  void* d_workspace, int64_t workspace_bytes, void* stream);
+
 /* Waits for `stream`, reads the plan's status word into *device_status
  * (MFR_STATUS_* bits) and clears it.  Returns MFR_OK or a CUDA error code. */
 int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_status);

@@ -71,6 +71,8 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_plan_info": (_I, [_VP, ctypes.POINTER(PlanInfo)]),
     "moe_finalize_rmsnorm_launch_floor": (_I, [_VP, _VP]),
     "moe_finalize_rmsnorm_bench_producer": (_I, [_VP, _VP, _I64, _I64, ctypes.c_longlong, _I, _VP]),
+    "moe_finalize_rmsnorm_host_workspace_bytes": (_I64, [_VP]),
+    "moe_finalize_rmsnorm_run_host": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _VP, _I64, _VP]),
     "moe_finalize_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
     "moe_finalize_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_finalize_rmsnorm_run_noalloc": (_I, [_I64, _I64, _I, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _I,
@@ -208,6 +210,26 @@ class Plan:
         _check(self._lib.moe_finalize_rmsnorm_launch_floor(self._h, _stream_handle(stream)),
                "moe_finalize_rmsnorm_launch_floor")
 
+    def host_workspace_bytes(self) -> int:
+        return int(self._lib.moe_finalize_rmsnorm_host_workspace_bytes(self._h))
+
+    def run_host(self, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, eps: float,
+                 out, workspace, stream=None) -> None:
+        """End to end from host tensors (pinned for asynchronous copies):
+        inputs copied into `workspace` (a device uint8 tensor of at least
+        host_workspace_bytes()), the kernel, outputs copied back, all on
+        `stream` (C: moe_finalize_rmsnorm_run_host)."""
+        for name, t in (("expert_out", expert_out), ("permuted_row_of", permuted_row_of),
+                        ("topk_weights", topk_weights), ("residual_in", residual_in),
+                        ("residual_out", residual_out), ("gamma", gamma), ("out", out)):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host tensor")
+        code = self._lib.moe_finalize_rmsnorm_run_host(
+            self._h, _ptr(expert_out), _ptr(permuted_row_of), _ptr(topk_weights), _ptr(residual_in),
+            _ptr(residual_out), _ptr(gamma), ctypes.c_float(eps), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        _check(code, "moe_finalize_rmsnorm_run_host")
+
     def get_status(self, stream=None) -> int:
         st = ctypes.c_int(0)
         _check(self._lib.moe_finalize_rmsnorm_get_status(self._h, _stream_handle(stream), ctypes.byref(st)),
@@ -301,21 +323,12 @@ def moe_finalize_residual_rmsnorm(expert_out, permuted_row_of, topk_weights, res
     return residual_out, out
 
 
-def finalize_residual_rmsnorm_host(plan: Plan, host_in: dict, dev: dict, host_out: dict, stream=None):
-    """End-to-end call on host buffers: copies the step's inputs from pinned
-    host memory to the device buffers in `dev`, runs the plan, and copies
-    residual_out and out back into pinned host memory, all on one stream.
-    Returns (h2d_bytes, d2h_bytes)."""
-    import torch
-    s = torch.cuda.current_stream() if stream is None else stream
-    h2d = 0
-    with torch.cuda.stream(s):
-        for key in ("expert_out", "permuted_row_of", "topk_weights", "residual", "gamma"):
-            dev[key].copy_(host_in[key], non_blocking=True)
-            h2d += host_in[key].numel() * host_in[key].element_size()
-        plan.run(dev["expert_out"], dev["permuted_row_of"], dev["topk_weights"], dev["residual"],
-                 dev["residual_out"], dev["gamma"], host_in["eps"], dev["out"], s, validate=False)
-        host_out["residual_out"].copy_(dev["residual_out"], non_blocking=True)
-        host_out["out"].copy_(dev["out"], non_blocking=True)
+def finalize_residual_rmsnorm_host(plan: Plan, host_in: dict, host_out: dict, workspace, stream=None):
+    """One end-to-end call on host buffers through the C ABI
+    (moe_finalize_rmsnorm_run_host).  Returns (h2d_bytes, d2h_bytes) moved."""
+    plan.run_host(host_in["expert_out"], host_in["permuted_row_of"], host_in["topk_weights"], host_in["residual"],
+                  host_out["residual_out"], host_in["gamma"], host_in["eps"], host_out["out"], workspace, stream)
+    h2d = sum(host_in[k].numel() * host_in[k].element_size()
+              for k in ("expert_out", "permuted_row_of", "topk_weights", "residual", "gamma"))
     d2h = sum(host_out[k].numel() * host_out[k].element_size() for k in ("residual_out", "out"))
     return h2d, d2h

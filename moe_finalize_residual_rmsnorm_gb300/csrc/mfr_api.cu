@@ -389,6 +389,92 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int3
     return MFR_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Device workspace of run_host: every tensor of one call, each 256-byte aligned.
+struct HostLayout {
+    size_t e, idx, w, res_in, res_out, gamma, out, total;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+HostLayout host_layout(const mfr_plan_s* p) {
+    HostLayout l{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) { const size_t at = off; off += align256(bytes); return at; };
+    l.e = take(static_cast<size_t>(p->R * p->H) * 2);
+    l.idx = take(static_cast<size_t>(p->T * p->k) * 4);
+    l.w = take(static_cast<size_t>(p->T * p->k) * 4);
+    l.res_in = take(static_cast<size_t>(p->T * p->H) * 4);
+    l.res_out = take(static_cast<size_t>(p->T * p->H) * 4);
+    l.gamma = take(static_cast<size_t>(p->H) * 2);
+    l.out = take(static_cast<size_t>(p->T * p->H) * 2);
+    l.total = off;
+    return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t moe_finalize_rmsnorm_host_workspace_bytes(mfr_plan_t plan) {
+    if (!plan || !plan->fused) return -1;
+    return static_cast<int64_t>(host_layout(plan).total);
+}
+
+int moe_finalize_rmsnorm_run_host(mfr_plan_t plan, const void* h_expert_out, const int32_t* h_permuted_row_of,
+                                  const float* h_topk_weights, const float* h_residual_in, float* h_residual_out,
+                                  const void* h_gamma, float eps, void* h_out, void* d_workspace,
+                                  int64_t workspace_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    if (!plan->fused) return fail(MFR_ERR_INVALID_ARG, "this plan was made by moe_finalize_plan");
+    if (plan->T == 0) return MFR_OK;
+    const HostLayout L = host_layout(plan);
+    if (!d_workspace || workspace_bytes < static_cast<int64_t>(L.total))
+        return fail(MFR_ERR_INVALID_ARG, "workspace of %lld bytes is smaller than the %llu the plan needs",
+                    (long long)workspace_bytes, (unsigned long long)L.total);
+    if (!aligned(d_workspace, 256)) return fail(MFR_ERR_MISALIGNED, "the workspace must be 256-byte aligned");
+    if (!h_permuted_row_of || !h_topk_weights || !h_residual_in || !h_residual_out || !h_gamma || !h_out ||
+        (plan->R > 0 && !h_expert_out))
+        return fail(MFR_ERR_INVALID_ARG, "a required host pointer is NULL");
+    const int64_t T = plan->T, H = plan->H, R = plan->R;
+    const int k = plan->k;
+    unsigned char* ws = static_cast<unsigned char*>(d_workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    struct Copy { void* dst; const void* src; size_t bytes; cudaMemcpyKind kind; };
+    const Copy in[] = {
+        {ws + L.e, h_expert_out, static_cast<size_t>(R * H) * 2, cudaMemcpyHostToDevice},
+        {ws + L.idx, h_permuted_row_of, static_cast<size_t>(T * k) * 4, cudaMemcpyHostToDevice},
+        {ws + L.w, h_topk_weights, static_cast<size_t>(T * k) * 4, cudaMemcpyHostToDevice},
+        {ws + L.res_in, h_residual_in, static_cast<size_t>(T * H) * 4, cudaMemcpyHostToDevice},
+        {ws + L.gamma, h_gamma, static_cast<size_t>(H) * 2, cudaMemcpyHostToDevice},
+    };
+    for (const Copy& c : in) {
+        if (c.bytes == 0) continue;
+        const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, c.kind, s);
+        if (e != cudaSuccess) { cudaGetLastError(); return fail_cuda(MFR_ERR_CUDA, "host-to-device copy", e); }
+    }
+    const int rc = moe_finalize_rmsnorm_run(plan, R > 0 ? ws + L.e : nullptr,
+                                            reinterpret_cast<const int32_t*>(ws + L.idx),
+                                            reinterpret_cast<const float*>(ws + L.w),
+                                            reinterpret_cast<const float*>(ws + L.res_in),
+                                            reinterpret_cast<float*>(ws + L.res_out), ws + L.gamma, eps,
+                                            ws + L.out, stream);
+    if (rc != MFR_OK) return rc;
+    const Copy outc[] = {
+        {h_residual_out, ws + L.res_out, static_cast<size_t>(T * H) * 4, cudaMemcpyDeviceToHost},
+        {h_out, ws + L.out, static_cast<size_t>(T * H) * 2, cudaMemcpyDeviceToHost},
+    };
+    for (const Copy& c : outc) {
+        const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, c.kind, s);
+        if (e != cudaSuccess) { cudaGetLastError(); return fail_cuda(MFR_ERR_CUDA, "device-to-host copy", e); }
+    }
+    return MFR_OK;
+}
+
 int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_status) {
     g_last_error[0] = '\0';
     if (!plan || !device_status) return fail(MFR_ERR_INVALID_ARG, "plan and device_status must not be NULL");
