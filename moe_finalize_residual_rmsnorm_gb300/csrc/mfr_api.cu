@@ -74,6 +74,7 @@ int auto_cluster(int chunks) {
 // persistent ring kernel, whose per-SM pipeline needs enough tokens per SM.
 constexpr int64_t kClusterMaxElems = int64_t(1) << 18;
 constexpr int64_t kRowsMaxElems = int64_t(3) << 20;
+constexpr int64_t kEarlyTriggerMaxElems = int64_t(1) << 19;
 constexpr int kMaxStages = 8;
 
 }  // namespace
@@ -172,6 +173,10 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     }
     if (variant != MFR_VARIANT_CLUSTER) csize = 1;
     l.variant = variant;
+    // Signal dependents at kernel entry only while this grid is small: a
+    // large grid would let the next kernel park CTAs on every SM for the
+    // whole call (the ring kernel never signals early, see mfr_stream.cu).
+    l.early_trigger = (variant != MFR_VARIANT_STREAM && T * H <= kEarlyTriggerMaxElems) ? 1 : 0;
 
     if (variant == MFR_VARIANT_STREAM) {
         if (stages < 2)
@@ -294,6 +299,7 @@ int moe_finalize_run(mfr_plan_t plan, const void* expert_out, const int32_t* per
     p.H = static_cast<int>(H);
     p.k = k;
     p.sentinel = plan->opt.sentinel_skip ? 1 : 0;
+    p.early_trigger = plan->launch.early_trigger;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = plan->launch.variant == MFR_VARIANT_STREAM ? mfr::stream_launch(p, plan->launch, s)
                                                    : mfr::rows_launch(p, plan->launch, s);
@@ -369,6 +375,7 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int3
     p.k = k;
     p.eps = eps;
     p.sentinel = plan->opt.sentinel_skip ? 1 : 0;
+    p.early_trigger = plan->launch.early_trigger;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = plan->launch.variant == MFR_VARIANT_STREAM ? mfr::stream_launch(p, plan->launch, s)

@@ -23,6 +23,7 @@ struct Params {
     int k;
     float eps;
     int sentinel;                   // 1: a negative index is a skipped non-local slot, not an error
+    int early_trigger;              // 1: signal dependents at kernel entry; 0: after the loads
 };
 
 // Launch geometry fixed by the plan.
@@ -37,6 +38,7 @@ struct Launch {
     int pdl;          // programmatic stream serialization
     int stages;       // MFR_VARIANT_STREAM: shared-memory ring depth
     int fused;        // 1: residual + RMSNorm; 0: plain finalize (out = bf16(sum))
+    int early_trigger;  // 1: signal dependents at kernel entry (small grids only)
 };
 
 constexpr int kMaxK = 16;         // slots per token

@@ -4,7 +4,10 @@
 // (MFR_VARIANT_CLUSTER).
 //
 // Per token t, for the columns this CTA owns:
-//   trigger   : let the next kernel in the stream start its prologue
+//   trigger   : let the next kernel in the stream start its prologue — at
+//               entry when the grid is small (few tokens: its CTAs leave room),
+//               else after the loads, so a following kernel does not park CTAs
+//               on every SM for the whole call
 //   prologue  : slot indices and weights of t, gamma; ask L2 to prefetch the
 //               CTA's row and residual segments             (before the PDL wait)
 //   wait      : the producer of expert_out / residual_in has finished
@@ -55,7 +58,8 @@ rows_kernel(const Params p, const int csize)
     __shared__ float s_warp[kRowsMaxThreads / 32];
     __shared__ float s_cta[16];
 
-    pdl_launch_dependents();   // the next kernel may start its prologue now
+    if (p.early_trigger)
+        pdl_launch_dependents();   // the next kernel may start its prologue now
     // cluster exchange: every CTA will receive csize partial sums (4 bytes
     // each) on s_bar; peers send only after the cluster barrier below, which
     // also publishes the barrier's initialisation
@@ -149,6 +153,9 @@ rows_kernel(const Params p, const int csize)
             }
         }
     }
+
+    if (!p.early_trigger)
+        pdl_launch_dependents();   // every load of this CTA has landed
 
     if constexpr (!FUSED) {
         // ---- plain finalize: out = bf16(acc) --------------------------------
