@@ -85,6 +85,19 @@ class Oracle:
         lib.mfr_oracle_finalize_residual_rmsnorm.restype = i64
         lib.mfr_oracle_finalize_only.argtypes = [i64, i64, i64, i64, p, p, p, p, p, i64]
         lib.mfr_oracle_finalize_only.restype = i64
+        lib.mfr_oracle_e4m3_from_f64.argtypes = [ctypes.c_double]
+        lib.mfr_oracle_e4m3_from_f64.restype = ctypes.c_uint8
+        lib.mfr_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.mfr_oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.mfr_oracle_e2m1_from_f64.argtypes = [ctypes.c_double]
+        lib.mfr_oracle_e2m1_from_f64.restype = ctypes.c_uint8
+        lib.mfr_oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.mfr_oracle_e2m1_to_f64.restype = ctypes.c_double
+        lib.mfr_oracle_nvfp4_quantize.argtypes = [i64, i64, p, ctypes.c_float, p, p]
+        lib.mfr_oracle_nvfp4_quantize.restype = None
+        lib.mfr_oracle_finalize_residual_rmsnorm_nvfp4.argtypes = [
+            i64, i64, i64, i64, p, p, p, p, p, ctypes.c_float, ctypes.c_float, p, p, p, p, i64, p, p]
+        lib.mfr_oracle_finalize_residual_rmsnorm_nvfp4.restype = i64
         self.lib = lib
         self.path = path
 
@@ -178,6 +191,68 @@ class Oracle:
         return out, int(bad)
 
 
+    # -- NVFP4 ----------------------------------------------------------------
+    def e4m3_from_f64(self, x) -> np.ndarray:
+        f = np.vectorize(self.lib.mfr_oracle_e4m3_from_f64, otypes=[np.uint8])
+        return f(np.asarray(x, dtype=np.float64))
+
+    def e4m3_to_f64(self, b) -> np.ndarray:
+        f = np.vectorize(self.lib.mfr_oracle_e4m3_to_f64, otypes=[np.float64])
+        return f(np.asarray(b, dtype=np.uint8))
+
+    def e2m1_from_f64(self, x) -> np.ndarray:
+        f = np.vectorize(self.lib.mfr_oracle_e2m1_from_f64, otypes=[np.uint8])
+        return f(np.asarray(x, dtype=np.float64))
+
+    def e2m1_to_f64(self, c) -> np.ndarray:
+        f = np.vectorize(self.lib.mfr_oracle_e2m1_to_f64, otypes=[np.float64])
+        return f(np.asarray(c, dtype=np.uint8))
+
+    def nvfp4_quantize(self, y, s_enc: float):
+        """y float32 [n, H] (H % 16 == 0) -> (packed codes uint8 [n, H/2],
+        block scales uint8 [n, H/16])."""
+        y = _c(y, np.float32)
+        n, H = y.shape
+        assert H % 16 == 0
+        q = np.empty((n, H // 2), dtype=np.uint8)
+        sf = np.empty((n, H // 16), dtype=np.uint8)
+        self.lib.mfr_oracle_nvfp4_quantize(n, H, _ptr(y), ctypes.c_float(s_enc), _ptr(q), _ptr(sf))
+        return q, sf
+
+    def finalize_residual_rmsnorm_nvfp4(self, expert_out_bits, permuted_row_of, topk_weights, residual_in,
+                                        gamma_bits, eps: float, s_enc: float,
+                                        tokens: Optional[Sequence[int]] = None):
+        """The path with the NVFP4 epilogue.  Returns (residual_out float32
+        [n, H], packed codes [n, H/2], block scales [n, H/16], bad slots)."""
+        E = _c(expert_out_bits, np.uint16)
+        idx = _c(permuted_row_of, np.int32)
+        w = _c(topk_weights, np.float32)
+        res = _c(residual_in, np.float32)
+        g = _c(gamma_bits, np.uint16)
+        R, H = E.shape
+        T, k = idx.shape
+        assert H % 16 == 0
+        tk, n = self._tokens(tokens, T)
+        res_out = np.empty((n, H), dtype=np.float32)
+        q = np.empty((n, H // 2), dtype=np.uint8)
+        sf = np.empty((n, H // 16), dtype=np.uint8)
+        ys = np.empty(H, dtype=np.float64)
+        y32 = np.empty(H, dtype=np.float32)
+        bad = self.lib.mfr_oracle_finalize_residual_rmsnorm_nvfp4(
+            T, H, k, R, _ptr(E), _ptr(idx), _ptr(w), _ptr(res), _ptr(g), ctypes.c_float(eps),
+            ctypes.c_float(s_enc), _ptr(res_out), _ptr(q), _ptr(sf), _ptr(tk), n, _ptr(ys), _ptr(y32))
+        return res_out, q, sf, int(bad)
+
+
+def unpack_e2m1(q_packed: np.ndarray) -> np.ndarray:
+    """[n, H/2] packed bytes -> [n, H] codes (element 2j = low nibble)."""
+    q = np.asarray(q_packed, dtype=np.uint8)
+    out = np.empty(q.shape[:-1] + (q.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = q & 0xF
+    out[..., 1::2] = q >> 4
+    return out
+
+
 _default: Optional[Oracle] = None
 _lock = threading.Lock()
 
@@ -208,3 +283,11 @@ def finalize_residual_rmsnorm(*a, **kw):
 
 def finalize_only(*a, **kw):
     return default().finalize_only(*a, **kw)
+
+
+def nvfp4_quantize(*a, **kw):
+    return default().nvfp4_quantize(*a, **kw)
+
+
+def finalize_residual_rmsnorm_nvfp4(*a, **kw):
+    return default().finalize_residual_rmsnorm_nvfp4(*a, **kw)

@@ -228,3 +228,139 @@ int64_t mfr_oracle_finalize_only(int64_t T, int64_t H, int64_t k, int64_t R,
     }
     return bad;
 }
+
+/* ---- NVFP4 quantisation of the normalised output ---------------------------
+ *
+ * The PR 6544 analysis (section 2.3) names an RMSNorm + NVFP4 quantisation
+ * fusion but not the format.  The format used here is the public NVFP4
+ * description: 4-bit E2M1 elements (sign, 2 exponent bits with bias 1, 1
+ * mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), one E4M3 scale per
+ * block of 16 consecutive elements of a row, and one FP32 tensor scale s_enc
+ * chosen by the caller.  For a block with elements y_i (FP32):
+ *     amax = max |y_i|
+ *     sf   = E4M3( (amax / 6) * s_enc )        nearest-even, saturating at 448
+ *     dec  = value(sf) / s_enc                 (the block's decode scale)
+ *     enc  = sf == 0 ? 0 : 1 / dec
+ *     q_i  = E2M1( y_i * enc )                 nearest-even, saturating at 6
+ * and y_i is recovered as value(q_i) * value(sf) / s_enc.  The divisions and
+ * products are single FP32 operations, as the kernel performs them, so that
+ * both sides take the integer decisions in the same precision.  Codes are
+ * packed two per byte, element 2j in the low nibble of byte j.
+ */
+
+/* E4M3: bias 7, 3 mantissa bits, normal exponents -6..8, subnormal spacing
+ * 2^-9, largest finite 448, no infinities.  Nearest-even; magnitudes above
+ * 448 saturate to 448; NaN gives 0x7F. */
+uint8_t mfr_oracle_e4m3_from_f64(double x)
+{
+    uint8_t sign = signbit(x) ? 0x80u : 0u;
+    if (isnan(x))
+        return 0x7Fu;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);
+    int lead = e - 1;
+    if (lead < -6)
+        lead = -6;
+    double spacing = ldexp(1.0, lead - 3);
+    double r = nearbyint(a / spacing) * spacing;
+    if (r > 448.0)
+        r = 448.0;
+    if (r == 0.0)
+        return sign;
+    (void)frexp(r, &e);
+    lead = e - 1;
+    if (lead < -6)                                   /* subnormal: units of 2^-9 */
+        return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+    int mant = (int)(r / ldexp(1.0, lead - 3)) - 8;  /* 0..7 */
+    return (uint8_t)(sign | (uint8_t)(((lead + 7) << 3) | mant));
+}
+
+double mfr_oracle_e4m3_to_f64(uint8_t b)
+{
+    double s = (b & 0x80u) ? -1.0 : 1.0;
+    int ef = (b >> 3) & 0xF, m = b & 7;
+    if (ef == 0xF && m == 7)
+        return NAN;
+    if (ef == 0)
+        return s * m * ldexp(1.0, -9);
+    return s * (8 + m) * ldexp(1.0, ef - 7 - 3);
+}
+
+static const double k_e2m1_mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* E2M1: the nearest of the eight magnitudes; on a tie the code whose mantissa
+ * bit is 0 (codes 0, 2, 4, 6); anything beyond 6 gives 6.  Sign in bit 3. */
+uint8_t mfr_oracle_e2m1_from_f64(double x)
+{
+    uint8_t sign = signbit(x) ? 0x8u : 0u;
+    if (isnan(x))
+        return 0x7u;
+    double a = fabs(x);
+    int best = 0;
+    for (int i = 1; i < 8; ++i) {
+        double d = fabs(a - k_e2m1_mag[i]), db = fabs(a - k_e2m1_mag[best]);
+        if (d < db || (d == db && (i & 1) == 0 && (best & 1) == 1))
+            best = i;
+    }
+    return (uint8_t)(sign | best);
+}
+
+double mfr_oracle_e2m1_to_f64(uint8_t c)
+{
+    return ((c & 0x8u) ? -1.0 : 1.0) * k_e2m1_mag[c & 7];
+}
+
+/* Quantises n rows of width H (H a multiple of 16) as described above.
+ * q_packed: n x H/2 bytes; sf: n x H/16 bytes. */
+void mfr_oracle_nvfp4_quantize(int64_t n, int64_t H, const float* y, float s_enc,
+                               uint8_t* q_packed, uint8_t* sf)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        for (int64_t b = 0; b < H / 16; ++b) {
+            const float* yb = y + i * H + b * 16;
+            float amax = 0.0f;
+            for (int j = 0; j < 16; ++j)
+                if (fabsf(yb[j]) > amax)
+                    amax = fabsf(yb[j]);
+            float v = (amax / 6.0f) * s_enc;
+            uint8_t s8 = mfr_oracle_e4m3_from_f64((double)v);
+            float sv = (float)mfr_oracle_e4m3_to_f64(s8);
+            float dec = sv / s_enc;
+            float enc = (s8 == 0) ? 0.0f : 1.0f / dec;
+            sf[i * (H / 16) + b] = s8;
+            for (int j = 0; j < 16; j += 2) {
+                float p0 = yb[j] * enc, p1 = yb[j + 1] * enc;
+                uint8_t c0 = mfr_oracle_e2m1_from_f64((double)p0);
+                uint8_t c1 = mfr_oracle_e2m1_from_f64((double)p1);
+                q_packed[i * (H / 2) + b * 8 + j / 2] = (uint8_t)(c0 | (c1 << 4));
+            }
+        }
+    }
+}
+
+/* The whole path with the NVFP4 epilogue: the residual as above, RMSNorm in
+ * double, the normalised value rounded once to FP32 (the precision the
+ * quantiser works in), then quantised. */
+int64_t mfr_oracle_finalize_residual_rmsnorm_nvfp4(
+    int64_t T, int64_t H, int64_t k, int64_t R,
+    const uint16_t* expert_out, const int32_t* idx, const float* w,
+    const float* residual_in, const uint16_t* gamma, float eps, float s_enc,
+    float* residual_out, uint8_t* q_packed, uint8_t* sf,
+    const int64_t* tokens, int64_t ntokens, double* y_scratch, float* y32_scratch)
+{
+    int64_t bad = 0;
+    int64_t n = tokens ? ntokens : T;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        float* xr = residual_out + i * H;
+        bad += mfr_oracle_weighted_residual(T, H, k, R, expert_out, idx, w, residual_in, xr, &t, 1);
+        mfr_oracle_rmsnorm_f64(1, H, xr, gamma, eps, y_scratch);
+        for (int64_t h = 0; h < H; ++h)
+            y32_scratch[h] = (float)y_scratch[h];
+        mfr_oracle_nvfp4_quantize(1, H, y32_scratch, s_enc, q_packed + i * (H / 2), sf + i * (H / 16));
+    }
+    return bad;
+}

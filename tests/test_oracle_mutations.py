@@ -3,7 +3,7 @@
 Each case copies the oracle's C source, plants one plausible mistake (a
 dropped term, a wrong sign, a wrong index, a misplaced eps, a wrong rounding,
 a reversed slot order ...), compiles the copy on the CPU, and runs every pin
-of tests/test_oracle.py against it.  At least one pin must fail.  The real
+of tests/test_oracle.py and tests/test_oracle_nvfp4.py against it.  At least one pin must fail.  The real
 oracle is never modified.
 """
 import importlib.util
@@ -61,6 +61,15 @@ MUTATIONS = {
          "                    continue;\n                float e"),
         ("x[i * H + h] = residual_in[t * H + h] + acc;", "x[i * H + h] = acc;")],
     "bad_slots_not_counted": [("            ++bad;\n", "")],
+    "e4m3_truncates": [("    double r = nearbyint(a / spacing) * spacing;\n    if (r > 448.0)",
+                        "    double r = floor(a / spacing) * spacing;\n    if (r > 448.0)")],
+    "e4m3_no_saturation": [("    if (r > 448.0)\n        r = 448.0;", "")],
+    "e2m1_ties_up": [("(d == db && (i & 1) == 0 && (best & 1) == 1)", "(d == db)")],
+    "nibbles_swapped": [("(uint8_t)(c0 | (c1 << 4))", "(uint8_t)(c1 | (c0 << 4))")],
+    "scale_not_rounded": [("            float sv = (float)mfr_oracle_e4m3_to_f64(s8);",
+                           "            float sv = v;")],
+    "amax_over_8": [("            for (int j = 0; j < 16; ++j)\n                if (fabsf(yb[j]) > amax)",
+                     "            for (int j = 0; j < 8; ++j)\n                if (fabsf(yb[j]) > amax)")],
     "finalize_only_double_rounding": [
         ("out[i * H + h] = mfr_oracle_bf16_from_f64((double)acc);",
          "out[i * H + h] = mfr_oracle_bf16_from_f64((double)(acc * 1.0009765625f));")],
@@ -68,7 +77,14 @@ MUTATIONS = {
 
 
 def _load_pins():
-    spec = importlib.util.spec_from_file_location("oracle_pins", os.path.join(HERE, "test_oracle.py"))
+    runs = []
+    for fname in ("test_oracle.py", "test_oracle_nvfp4.py"):
+        runs += _pins_of(fname)
+    return runs
+
+
+def _pins_of(fname):
+    spec = importlib.util.spec_from_file_location(fname[:-3], os.path.join(HERE, fname))
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
     runs = []
