@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="prefill", choices=sorted(W.all_named()))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sweep", action="store_true", help="also time the decode and wide sweeps")
+    ap.add_argument("--variants", action="store_true",
+                    help="also time the plain finalize and the NVFP4 epilogue on the headline workload")
     ap.add_argument("--pdl-pairs", action="store_true",
                     help="also time producer -> finalize pairs with and without dependent launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -366,6 +368,8 @@ def run_ours(args):
         result["sweep"] = run_sweep(mfr, device, args)
     if args.pdl_pairs:
         result["pdl_pairs"] = run_pdl_pairs(mfr, device)
+    if args.variants:
+        result["variants"] = run_variants(mfr, device, wl, sets, args)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(host_copy(sets[0]), wl, args.cpu_seconds)
     if rank == 0:
@@ -477,6 +481,51 @@ def run_sweep(mfr, device, args):
         del E, idx, w, res, rout, out, base
         torch.cuda.empty_cache()
     return rows
+
+
+def run_variants(mfr, device, wl, sets, args):
+    """The other two outputs of the library on the headline workload, timed
+    like the main step (two alternating input sets, CUDA events):
+    plain finalize (bf16 sum, no residual or norm: k*H*2 + H*2 + k*8 bytes
+    per token) and the NVFP4 epilogue (residual + RMSNorm, output as E2M1
+    codes + E4M3 block scales: k*H*2 + H*8 + H/2 + H/16 + k*8 bytes)."""
+    T, H, k, R = wl.T, wl.H, wl.k, wl.R
+    steps = max(20, min(args.steps, 500))
+    stream = torch.cuda.Stream(device)
+    out = {}
+    fin = mfr.FinalizePlan(T, H, k, R, enable_pdl=not args.no_pdl)
+    fp4 = mfr.Nvfp4Plan(T, H, k, R, enable_pdl=not args.no_pdl)
+    q = [torch.empty((T, H // 2), dtype=torch.uint8, device=device) for _ in range(2)]
+    sf = [torch.empty((T, H // 16), dtype=torch.uint8, device=device) for _ in range(2)]
+    s_enc = 448.0 * 6.0 / 16.0
+
+    def fin_step(i):
+        d = sets[i & 1]
+        fin.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["out"], stream, validate=False)
+
+    def fp4_step(i):
+        d = sets[i & 1]
+        fp4.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["residual"], d["residual_out"],
+                d["gamma"], d["eps"], s_enc, q[i & 1], sf[i & 1], stream, validate=False)
+
+    for name, fn, nbytes in (("finalize_only", fin_step, T * (k * H * 2 + H * 2 + k * 8)),
+                             ("nvfp4_epilogue", fp4_step, T * (k * H * 2 + H * 8 + H // 2 + H // 16 + k * 8))):
+        for i in range(5):
+            fn(i)
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            fn(i)
+        b.record(stream)
+        b.synchronize()
+        us = a.elapsed_time(b) * 1e3 / steps
+        out[name] = {"us_per_call": round(us, 2), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "bytes_per_call": int(nbytes), "steps": steps,
+                     "variant": (fin if name == "finalize_only" else fp4).info()["variant_name"]}
+    if fin.get_status(stream) or fp4.get_status(stream):
+        raise RuntimeError("status word set while timing the variants")
+    return out
 
 
 def run_pdl_pairs(mfr, device):

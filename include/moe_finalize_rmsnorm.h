@@ -147,6 +147,34 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan,
                              float* residual_out, const void* gamma, float eps,
                              void* out, void* stream);
 
+/* ---- residual + RMSNorm with an NVFP4 output ----------------------------
+ * The same fused call, but the normalised FP32 values are written as NVFP4
+ * for the next GEMM instead of bf16: "FlashInfer, Muse-Spark-Open을 위한
+ * 융합 정규화 및 TP/EP MoE 최적화로 성능 극대화" (flashinfer PR 6544 analysis),
+ * section 2.3, fuses RMSNorm with NVFP4 quantisation; the format follows the
+ * public NVFP4 description.  For each block of 16 consecutive columns of a
+ * token, with y the FP32 value (x * rsqrt(mean(x^2) + eps)) * gamma:
+ *   amax = max |y|;  sf = E4M3((amax / 6) * s_enc)   nearest-even, saturating
+ *   dec = value(sf) / s_enc;  enc = sf == 0 ? 0 : 1 / dec
+ *   q   = E2M1(y * enc)                              nearest-even, saturating
+ * so that y ~ value(q) * value(sf) / s_enc.  Each step is one FP32 operation.
+ *  s_enc   the FP32 tensor scale (> 0, finite); the usual choice is
+ *          448 * 6 / amax over the tensor, measured offline
+ *  out_q   device, uint8 [T, H/2], 4-byte aligned: two codes per byte,
+ *          column 2j in the low nibble of byte j
+ *  out_sf  device, uint8 [T, H/16]: E4M3 block scales, row-major (not the
+ *          swizzled layout some GEMMs read)
+ * residual_out is written as in moe_finalize_rmsnorm_run.  Needs H % 16 == 0.
+ * Plans come from moe_finalize_rmsnorm_nvfp4_plan (same arguments and
+ * options as moe_finalize_rmsnorm_plan) and run only with
+ * moe_finalize_rmsnorm_nvfp4_run. */
+int moe_finalize_rmsnorm_nvfp4_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                                    const mfr_options* opt);
+int moe_finalize_rmsnorm_nvfp4_run(mfr_plan_t plan, const void* expert_out,
+                                   const int32_t* permuted_row_of, const float* topk_weights,
+                                   const float* residual_in, float* residual_out, const void* gamma,
+                                   float eps, float s_enc, void* out_q, void* out_sf, void* stream);
+
 /* ---- plain finalize (no residual, no norm) ------------------------------
  * out[t, h] = bf16( sum_j fma(w[t,j], E[idx[t,j], h], .) ), the FP32 weighted
  * sum in slot order rounded once to bf16: the finalize kernel of

@@ -19,7 +19,7 @@ from typing import Optional
 from .build import LIBRARY, build as _build_library
 
 __all__ = [
-    "LIBRARY", "MFRError", "Plan", "FinalizePlan", "PlanInfo", "Options", "build", "load_library", "supports",
+    "LIBRARY", "MFRError", "Plan", "FinalizePlan", "Nvfp4Plan", "PlanInfo", "Options", "build", "load_library", "supports",
     "moe_finalize_residual_rmsnorm", "finalize_residual_rmsnorm_host", "exported_symbols",
     "VARIANT_AUTO", "VARIANT_CLUSTER", "VARIANT_ROWS", "VARIANT_STREAM", "STATUS_BAD_INDEX",
     "ERROR_CODES",
@@ -73,6 +73,8 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_bench_producer": (_I, [_VP, _VP, _I64, _I64, ctypes.c_longlong, _I, _VP]),
     "moe_finalize_rmsnorm_host_workspace_bytes": (_I64, [_VP]),
     "moe_finalize_rmsnorm_run_host": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _VP, _I64, _VP]),
+    "moe_finalize_rmsnorm_nvfp4_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
+    "moe_finalize_rmsnorm_nvfp4_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _F, _F, _VP, _VP, _VP]),
     "moe_finalize_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
     "moe_finalize_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_finalize_rmsnorm_run_noalloc": (_I, [_I64, _I64, _I, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _I,
@@ -252,6 +254,37 @@ class Plan:
 
     def __exit__(self, *exc):
         self.close()
+
+
+class Nvfp4Plan(Plan):
+    """Residual + RMSNorm with the normalised output written as NVFP4
+    (C: moe_finalize_rmsnorm_nvfp4_plan / moe_finalize_rmsnorm_nvfp4_run):
+    out_q uint8 [T, H/2] (two E2M1 codes per byte, even column in the low
+    nibble), out_sf uint8 [T, H/16] (E4M3 block scales), s_enc the FP32
+    tensor scale."""
+
+    _PLAN_FN = "moe_finalize_rmsnorm_nvfp4_plan"
+
+    def run(self, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, eps: float,
+            s_enc: float, out_q, out_sf, stream=None, *, validate: bool = True):
+        if validate:
+            import torch
+            T, H, k, R = self.T, self.H, self.k, self.R
+            for name, t, dt, shape in [("expert_out", expert_out, torch.bfloat16, (R, H)),
+                                       ("permuted_row_of", permuted_row_of, torch.int32, (T, k)),
+                                       ("topk_weights", topk_weights, torch.float32, (T, k)),
+                                       ("residual_in", residual_in, torch.float32, (T, H)),
+                                       ("residual_out", residual_out, torch.float32, (T, H)),
+                                       ("gamma", gamma, torch.bfloat16, (H,)),
+                                       ("out_q", out_q, torch.uint8, (T, H // 2)),
+                                       ("out_sf", out_sf, torch.uint8, (T, H // 16))]:
+                if t.dtype != dt or tuple(t.shape) != shape or not t.is_cuda or not t.is_contiguous():
+                    raise ValueError(f"{name}: expected contiguous CUDA {dt} {shape}")
+        code = self._lib.moe_finalize_rmsnorm_nvfp4_run(
+            self._h, _ptr(expert_out), _ptr(permuted_row_of), _ptr(topk_weights), _ptr(residual_in),
+            _ptr(residual_out), _ptr(gamma), ctypes.c_float(eps), ctypes.c_float(s_enc), _ptr(out_q),
+            _ptr(out_sf), _stream_handle(stream))
+        _check(code, "moe_finalize_rmsnorm_nvfp4_run")
 
 
 class FinalizePlan(Plan):

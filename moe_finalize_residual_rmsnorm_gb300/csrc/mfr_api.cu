@@ -21,7 +21,8 @@ struct mfr_plan_s {
     mfr_options opt;
     mfr::Launch launch;
     int* d_status;
-    bool fused;        // made by moe_finalize_rmsnorm_plan (true) or moe_finalize_plan (false)
+    bool fused;        // residual + RMSNorm (false: moe_finalize_plan's plain finalize)
+    bool fp4;          // made by moe_finalize_rmsnorm_nvfp4_plan: NVFP4 output
 };
 
 namespace {
@@ -107,7 +108,7 @@ namespace {
 
 // Shared by the fused plan (residual + RMSNorm) and the plain-finalize plan.
 int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mfr_options* opt,
-              bool fused) {
+              bool fused, bool fp4) {
     g_last_error[0] = '\0';
     if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
     *plan = nullptr;
@@ -150,6 +151,9 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     l.pdl = o.enable_pdl ? 1 : 0;
     l.grid_y = 1;
     l.fused = fused ? 1 : 0;
+    l.fp4 = fp4 ? 1 : 0;
+    if (fp4 && H % 16 != 0)
+        return fail(MFR_ERR_UNSUPPORTED_SHAPE, "NVFP4 output needs H %% 16 == 0 (H=%lld)", (long long)H);
     int variant = o.force_variant;
     int csize = o.cluster_size;
     // ring depth the bulk-copy kernel would get on this device
@@ -172,6 +176,9 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         if (csize < 2) csize = 2;
     }
     if (variant != MFR_VARIANT_CLUSTER) csize = 1;
+    // NVFP4 blocks of 16 columns must not straddle two CTAs of a cluster
+    while (fp4 && csize > 1 && (chunks / csize) % 2 != 0) csize /= 2;
+    if (variant == MFR_VARIANT_CLUSTER && csize < 2) variant = MFR_VARIANT_ROWS;
     l.variant = variant;
     // Signal dependents at kernel entry only while this grid is small: a
     // large grid would let the next kernel park CTAs on every SM for the
@@ -190,7 +197,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         l.grid_x = static_cast<int>(T < sms ? (T > 0 ? T : 1) : sms);
         // the attribute is per kernel, shared by every plan: always the device
         // maximum, so a plan with a deeper ring never loses its setting
-        if ((e = mfr::stream_prepare(static_cast<int>(H), fused, ring_budget)) != cudaSuccess) {
+        if ((e = mfr::stream_prepare(static_cast<int>(H), fused, fp4, ring_budget)) != cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }
@@ -245,6 +252,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     p->launch = l;
     p->d_status = status;
     p->fused = fused;
+    p->fp4 = fp4;
     *plan = p;
     return MFR_OK;
 }
@@ -255,11 +263,16 @@ extern "C" {
 
 int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
                               const mfr_options* opt) {
-    return make_plan(plan, T, H, k, R, opt, true);
+    return make_plan(plan, T, H, k, R, opt, true, false);
+}
+
+int moe_finalize_rmsnorm_nvfp4_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                                    const mfr_options* opt) {
+    return make_plan(plan, T, H, k, R, opt, true, true);
 }
 
 int moe_finalize_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mfr_options* opt) {
-    return make_plan(plan, T, H, k, R, opt, false);
+    return make_plan(plan, T, H, k, R, opt, false, false);
 }
 
 int moe_finalize_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
@@ -319,26 +332,32 @@ int moe_finalize_run(mfr_plan_t plan, const void* expert_out, const int32_t* per
     return MFR_OK;
 }
 
-int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
-                             const float* topk_weights, const float* residual_in, float* residual_out,
-                             const void* gamma, float eps, void* out, void* stream) {
-    g_last_error[0] = '\0';
-    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
-    if (!plan->fused) return fail(MFR_ERR_INVALID_ARG, "this plan was made by moe_finalize_plan");
+}  // extern "C"
+
+namespace {
+
+// Checks and launches one fused call: bf16 output (out) or NVFP4 output
+// (out_q, out_sf, s_enc) according to the plan.
+int fused_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
+              const float* topk_weights, const float* residual_in, float* residual_out, const void* gamma,
+              float eps, void* out, void* out_q, void* out_sf, float s_enc, void* stream) {
     const int64_t T = plan->T, H = plan->H, R = plan->R;
     const int k = plan->k;
     if (T == 0) return MFR_OK;
-    if (!permuted_row_of || !topk_weights || !residual_in || !residual_out || !gamma || !out ||
-        (R > 0 && !expert_out))
+    const bool fp4 = plan->fp4;
+    if (!permuted_row_of || !topk_weights || !residual_in || !residual_out || !gamma ||
+        (fp4 ? (!out_q || !out_sf) : !out) || (R > 0 && !expert_out))
         return fail(MFR_ERR_INVALID_ARG, "a required pointer is NULL");
     if (!std::isfinite(eps) || eps < 0.f)
         return fail(MFR_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (fp4 && (!std::isfinite(s_enc) || s_enc <= 0.f))
+        return fail(MFR_ERR_INVALID_ARG, "the NVFP4 tensor scale must be finite and > 0");
     if (!aligned(expert_out, 16) || !aligned(residual_in, 16) || !aligned(residual_out, 16) ||
-        !aligned(gamma, 16) || !aligned(out, 16))
+        !aligned(gamma, 16) || (!fp4 && !aligned(out, 16)))
         return fail(MFR_ERR_MISALIGNED, "expert_out, residual_in, residual_out, gamma and out must be "
                                         "16-byte aligned");
-    if (!aligned(permuted_row_of, 4) || !aligned(topk_weights, 4))
-        return fail(MFR_ERR_MISALIGNED, "permuted_row_of and topk_weights must be 4-byte aligned");
+    if (!aligned(permuted_row_of, 4) || !aligned(topk_weights, 4) || (fp4 && !aligned(out_q, 4)))
+        return fail(MFR_ERR_MISALIGNED, "permuted_row_of, topk_weights and out_q must be 4-byte aligned");
 
     const size_t n_res = static_cast<size_t>(T * H) * sizeof(float);
     const size_t n_out = static_cast<size_t>(T * H) * 2;
@@ -349,10 +368,18 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int3
     if (overlaps(residual_out, n_res, expert_out, n_e) || overlaps(residual_out, n_res, permuted_row_of, n_tk) ||
         overlaps(residual_out, n_res, topk_weights, n_tk) || overlaps(residual_out, n_res, gamma, H * 2))
         return fail(MFR_ERR_INVALID_ARG, "residual_out overlaps an input");
-    if (overlaps(out, n_out, expert_out, n_e) || overlaps(out, n_out, permuted_row_of, n_tk) ||
-        overlaps(out, n_out, topk_weights, n_tk) || overlaps(out, n_out, residual_in, n_res) ||
-        overlaps(out, n_out, residual_out, n_res) || overlaps(out, n_out, gamma, H * 2))
-        return fail(MFR_ERR_INVALID_ARG, "out overlaps another argument");
+    // every output region against every other argument
+    const void* outs[2] = {fp4 ? out_q : out, fp4 ? out_sf : nullptr};
+    const size_t out_bytes[2] = {fp4 ? n_out / 4 : n_out, fp4 ? static_cast<size_t>(T * H) / 16 : 0};
+    for (int o = 0; o < 2; ++o) {
+        if (!outs[o]) continue;
+        if (overlaps(outs[o], out_bytes[o], expert_out, n_e) || overlaps(outs[o], out_bytes[o], permuted_row_of, n_tk) ||
+            overlaps(outs[o], out_bytes[o], topk_weights, n_tk) || overlaps(outs[o], out_bytes[o], residual_in, n_res) ||
+            overlaps(outs[o], out_bytes[o], residual_out, n_res) || overlaps(outs[o], out_bytes[o], gamma, H * 2))
+            return fail(MFR_ERR_INVALID_ARG, "an output overlaps another argument");
+    }
+    if (fp4 && overlaps(out_q, out_bytes[0], out_sf, out_bytes[1]))
+        return fail(MFR_ERR_INVALID_ARG, "out_q and out_sf overlap");
 
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -368,6 +395,9 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int3
     p.residual_out = residual_out;
     p.gamma = static_cast<const uint16_t*>(gamma);
     p.out = static_cast<uint16_t*>(out);
+    p.out_q = static_cast<uint8_t*>(out_q);
+    p.out_sf = static_cast<uint8_t*>(out_sf);
+    p.s_enc = s_enc;
     p.status = plan->d_status;
     p.T = T;
     p.R = R;
@@ -394,6 +424,32 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int3
             return fail(MFR_ERR_BAD_INDEX, "a permuted_row_of entry was outside [0, %lld)", (long long)R);
     }
     return MFR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_finalize_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
+                             const float* topk_weights, const float* residual_in, float* residual_out,
+                             const void* gamma, float eps, void* out, void* stream) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    if (!plan->fused || plan->fp4)
+        return fail(MFR_ERR_INVALID_ARG, "this plan was not made by moe_finalize_rmsnorm_plan");
+    return fused_run(plan, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, eps, out,
+                     nullptr, nullptr, 0.f, stream);
+}
+
+int moe_finalize_rmsnorm_nvfp4_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
+                                   const float* topk_weights, const float* residual_in, float* residual_out,
+                                   const void* gamma, float eps, float s_enc, void* out_q, void* out_sf,
+                                   void* stream) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    if (!plan->fp4) return fail(MFR_ERR_INVALID_ARG, "this plan was not made by moe_finalize_rmsnorm_nvfp4_plan");
+    return fused_run(plan, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, eps,
+                     nullptr, out_q, out_sf, s_enc, stream);
 }
 
 }  // extern "C"
@@ -427,7 +483,7 @@ HostLayout host_layout(const mfr_plan_s* p) {
 extern "C" {
 
 int64_t moe_finalize_rmsnorm_host_workspace_bytes(mfr_plan_t plan) {
-    if (!plan || !plan->fused) return -1;
+    if (!plan || !plan->fused || plan->fp4) return -1;
     return static_cast<int64_t>(host_layout(plan).total);
 }
 
@@ -437,7 +493,8 @@ int moe_finalize_rmsnorm_run_host(mfr_plan_t plan, const void* h_expert_out, con
                                   int64_t workspace_bytes, void* stream) {
     g_last_error[0] = '\0';
     if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
-    if (!plan->fused) return fail(MFR_ERR_INVALID_ARG, "this plan was made by moe_finalize_plan");
+    if (!plan->fused || plan->fp4)
+        return fail(MFR_ERR_INVALID_ARG, "this plan was not made by moe_finalize_rmsnorm_plan");
     if (plan->T == 0) return MFR_OK;
     const HostLayout L = host_layout(plan);
     if (!d_workspace || workspace_bytes < static_cast<int64_t>(L.total))

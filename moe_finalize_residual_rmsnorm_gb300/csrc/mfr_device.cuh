@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "moe_finalize_rmsnorm.h"
 
@@ -128,6 +129,53 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---- NVFP4 ------------------------------------------------------------------------
+// E4M3 byte of v: nearest-even, magnitudes beyond 448 saturate to 448.
+__device__ __forceinline__ uint32_t e4m3_rn_sat(float v) {
+    uint16_t e;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(e) : "f"(v));
+    return e & 0xFFu;
+}
+
+// Value of an E4M3 byte (exact through f16).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(b)));
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// Two E2M1 codes (nearest-even, saturating at 6): lo in bits 3..0, hi in 7..4.
+// The instruction puts its first source in the upper nibble.
+__device__ __forceinline__ uint32_t e2m1x2_rn_sat(float lo, float hi) {
+    uint16_t q;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(q) : "f"(hi), "f"(lo));
+    return q & 0xFFu;
+}
+
+// NVFP4 of a 16-element block held by a lane pair (lanes 2m and 2m+1, eight
+// values each, lane 2m holding the first eight).  All 32 lanes must call it.
+//   amax = max |y|;  sf = E4M3((amax / 6) * s_enc);  dec = value(sf) / s_enc;
+//   enc = sf == 0 ? 0 : 1 / dec;  q_i = E2M1(y_i * enc)
+// Every step is one correctly rounded FP32 operation.  Returns this lane's
+// eight codes packed into 4 bytes (element 0 in the lowest nibble) and the
+// block's scale byte in *sf.
+__device__ __forceinline__ uint32_t nvfp4_block8(const float (&y)[8], float s_enc, uint32_t* sf) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(y[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    const uint32_t s8 = e4m3_rn_sat(__fmul_rn(__fdiv_rn(amax, 6.0f), s_enc));
+    const float dec = __fdiv_rn(e4m3_to_f32(s8), s_enc);
+    const float enc = (s8 == 0u) ? 0.f : __fdiv_rn(1.0f, dec);
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        w |= e2m1x2_rn_sat(__fmul_rn(y[2 * j], enc), __fmul_rn(y[2 * j + 1], enc)) << (8 * j);
+    *sf = s8;
+    return w;
 }
 
 // ---- reductions ------------------------------------------------------------------

@@ -16,6 +16,9 @@ struct Params {
     float* residual_out;            // [T, H]
     const uint16_t* gamma;          // bf16 bits [H]
     uint16_t* out;                  // bf16 bits [T, H]
+    uint8_t* out_q;                 // NVFP4 codes [T, H/2] (NVFP4 plans)
+    uint8_t* out_sf;                // NVFP4 block scales, E4M3 [T, H/16] (NVFP4 plans)
+    float s_enc;                    // NVFP4 tensor scale
     int* status;                    // device status word (MFR_STATUS_* bits)
     int64_t T;
     int64_t R;
@@ -38,6 +41,7 @@ struct Launch {
     int pdl;          // programmatic stream serialization
     int stages;       // MFR_VARIANT_STREAM: shared-memory ring depth
     int fused;        // 1: residual + RMSNorm; 0: plain finalize (out = bf16(sum))
+    int fp4;          // 1: the normalised output is written as NVFP4 instead of bf16
     int early_trigger;  // 1: signal dependents at kernel entry (small grids only)
 };
 
@@ -60,7 +64,7 @@ cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s);
 int stream_threads();
 int stream_stage_bytes(int k, bool fused);
 int stream_smem_bytes(int k, int nstages, bool fused);
-cudaError_t stream_prepare(int H, bool fused, int smem_bytes);
+cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes);
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s);
 
 }  // namespace mfr

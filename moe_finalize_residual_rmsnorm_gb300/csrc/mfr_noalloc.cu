@@ -73,7 +73,7 @@ int setup_device(int dev, DeviceSetup* out) {
         // one attribute per kernel instantiation (by column tiles per token),
         // set to the device maximum exactly as the planned path sets it
         for (int h : {4096, 8192, 16384}) {
-            if (mfr::stream_prepare(h, true, budget) != cudaSuccess) {
+            if (mfr::stream_prepare(h, true, false, budget) != cudaSuccess) {
                 cudaGetLastError();
                 return MFR_ERR_CUDA;
             }

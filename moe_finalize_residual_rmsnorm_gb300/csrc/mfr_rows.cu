@@ -22,7 +22,10 @@
 //               CTA pushes its partial into every peer's shared memory with
 //               st.async, counted on the peer's mbarrier (PR 4730 analysis,
 //               section 2: cluster exchange through distributed shared memory)
-//   normalise : y = (x * rsqrt(ss / H + eps)) * gamma, rounded to bf16
+//   normalise : y = (x * rsqrt(ss / H + eps)) * gamma, rounded to bf16, or
+//               (FP4) quantised to NVFP4: 16-element blocks with an E4M3
+//               scale, E2M1 codes (PR 6544 analysis, section 2.3: RMSNorm
+//               fused with NVFP4 quantisation)
 // With FUSED = false the kernel is the plain finalize of the PR 5319 page:
 // out = bf16(acc), no residual, no norm; the C CTAs of a token then split
 // the columns without a cluster (nothing to reduce).
@@ -41,7 +44,7 @@ namespace {
 
 // CPT: 16-byte column chunks per thread per row; SG: slots gathered together;
 // FUSED: residual + RMSNorm (true) or plain finalize (false).
-template <int CPT, int SG, bool FUSED>
+template <int CPT, int SG, bool FUSED, bool FP4>
 __global__ void __launch_bounds__(kRowsMaxThreads)
 rows_kernel(const Params p, const int csize)
 {
@@ -218,6 +221,25 @@ rows_kernel(const Params p, const int csize)
 
     // ---- y = (x * inv) * gamma -> bf16 ----------------------------------------
     const float inv = rsqrtf(tot / static_cast<float>(p.H) + p.eps);
+    if constexpr (FP4) {
+        // NVFP4: chunks c and c^1 (lanes tid and tid^1) form one 16-element block
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int c = tid + i * nthreads;
+            float gf[8], y[8];
+            unpack8(g[i], gf);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) y[q] = (c < nck) ? acc[i][q] * inv * gf[q] : 0.f;
+            uint32_t sf;
+            const uint32_t w = nvfp4_block8(y, p.s_enc, &sf);
+            if (c < nck) {
+                const int64_t col = col0 + static_cast<int64_t>(c) * 8;
+                *reinterpret_cast<uint32_t*>(p.out_q + t * (p.H / 2) + col / 2) = w;
+                if ((c & 1) == 0) p.out_sf[t * (p.H / 16) + col / 16] = static_cast<uint8_t>(sf);
+            }
+        }
+        return;
+    }
     uint16_t* out = p.out + t * p.H + col0;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
@@ -237,11 +259,15 @@ rows_kernel(const Params p, const int csize)
 
 using RowsKernel = void (*)(const Params, const int);
 
-RowsKernel rows_kernel_for(int cpt, bool fused) {
+RowsKernel rows_kernel_for(int cpt, bool fused, bool fp4) {
+    if (fp4 && !fused) return nullptr;
     switch (cpt) {
-        case 1: return fused ? rows_kernel<1, 8, true> : rows_kernel<1, 8, false>;
-        case 2: return fused ? rows_kernel<2, 8, true> : rows_kernel<2, 8, false>;
-        case 4: return fused ? rows_kernel<4, 2, true> : rows_kernel<4, 2, false>;
+        case 1: return fp4 ? rows_kernel<1, 8, true, true>
+                           : (fused ? rows_kernel<1, 8, true, false> : rows_kernel<1, 8, false, false>);
+        case 2: return fp4 ? rows_kernel<2, 8, true, true>
+                           : (fused ? rows_kernel<2, 8, true, false> : rows_kernel<2, 8, false, false>);
+        case 4: return fp4 ? rows_kernel<4, 2, true, true>
+                           : (fused ? rows_kernel<4, 2, true, false> : rows_kernel<4, 2, false, false>);
         default: return nullptr;
     }
 }
@@ -296,10 +322,10 @@ cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, floor_kernel, status);
 }
 
-bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt, true) != nullptr; }
+bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt, true, false) != nullptr; }
 
 cudaError_t rows_prepare(const Launch& l) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0);
     if (!k) return cudaErrorInvalidValue;
     if (l.cluster > 8 && l.fused)
         return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -307,7 +333,7 @@ cudaError_t rows_prepare(const Launch& l) {
 }
 
 cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];
@@ -316,7 +342,7 @@ cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
 }
 
 cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];

@@ -9,7 +9,7 @@
 // accumulate acc = fma(w_j, e_j, acc) in slot order, add the residual, write
 // residual_out, release the stage, and keep x in registers; after the last
 // tile of a token they reduce the sum of squares (warp butterfly, then warps
-// in index order) and write the bf16 output.
+// in index order) and write the bf16 output, or (FP4) its NVFP4 quantisation.
 //
 // With FUSED = false it is the plain finalize of the PR 5319 page: no
 // residual in the stages, out = bf16(acc) written tile by tile, no norm.
@@ -52,7 +52,7 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 // MAXTILES: upper bound on ceil(H / CB) for this instantiation;
 // FUSED: residual + RMSNorm (true) or plain finalize (false).
-template <int MAXTILES, bool FUSED>
+template <int MAXTILES, bool FUSED, bool FP4>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 stream_kernel(const Params p, const int nstages, const int stage_bytes)
 {
@@ -305,17 +305,38 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
         asm volatile("bar.sync 1, %0;" :: "r"(kStreamNT) : "memory");  // s_warp reusable
         if (stop) break;
         const float inv = rsqrtf(tot / static_cast<float>(H) + p.eps);
+        if constexpr (FP4) {
+            // NVFP4: lanes tid and tid^1 hold the two halves of a 16-element block
 #pragma unroll
-        for (int b = 0; b < MAXTILES; ++b) {
-            if (b >= ntiles) break;
-            const int col = b * kStreamCB + tid * 8;
-            if (col < H) {
-                uint4 o;
-                o.x = pack_bf16x2(x[b][0] * inv * bf16_lo(g[b][0]), x[b][1] * inv * bf16_hi(g[b][0]));
-                o.y = pack_bf16x2(x[b][2] * inv * bf16_lo(g[b][1]), x[b][3] * inv * bf16_hi(g[b][1]));
-                o.z = pack_bf16x2(x[b][4] * inv * bf16_lo(g[b][2]), x[b][5] * inv * bf16_hi(g[b][2]));
-                o.w = pack_bf16x2(x[b][6] * inv * bf16_lo(g[b][3]), x[b][7] * inv * bf16_hi(g[b][3]));
-                st_u4(p.out + t * H + col, o);
+            for (int b = 0; b < MAXTILES; ++b) {
+                if (b >= ntiles) break;
+                const int col = b * kStreamCB + tid * 8;
+                float y[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t gw = g[b][q >> 1];
+                    y[q] = (col < H) ? x[b][q] * inv * ((q & 1) ? bf16_hi(gw) : bf16_lo(gw)) : 0.f;
+                }
+                uint32_t sf;
+                const uint32_t w = nvfp4_block8(y, p.s_enc, &sf);
+                if (col < H) {
+                    *reinterpret_cast<uint32_t*>(p.out_q + t * (H / 2) + col / 2) = w;
+                    if ((tid & 1) == 0) p.out_sf[t * (H / 16) + col / 16] = static_cast<uint8_t>(sf);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < MAXTILES; ++b) {
+                if (b >= ntiles) break;
+                const int col = b * kStreamCB + tid * 8;
+                if (col < H) {
+                    uint4 o;
+                    o.x = pack_bf16x2(x[b][0] * inv * bf16_lo(g[b][0]), x[b][1] * inv * bf16_hi(g[b][0]));
+                    o.y = pack_bf16x2(x[b][2] * inv * bf16_lo(g[b][1]), x[b][3] * inv * bf16_hi(g[b][1]));
+                    o.z = pack_bf16x2(x[b][4] * inv * bf16_lo(g[b][2]), x[b][5] * inv * bf16_hi(g[b][2]));
+                    o.w = pack_bf16x2(x[b][6] * inv * bf16_lo(g[b][3]), x[b][7] * inv * bf16_hi(g[b][3]));
+                    st_u4(p.out + t * H + col, o);
+                }
             }
         }
     }
@@ -324,11 +345,17 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
 
 using StreamKernel = void (*)(const Params, const int, const int);
 
-StreamKernel stream_kernel_for(int H, bool fused) {
+template <int MAXTILES>
+StreamKernel pick(bool fused, bool fp4) {
+    if (fp4) return fused ? stream_kernel<MAXTILES, true, true> : nullptr;
+    return fused ? stream_kernel<MAXTILES, true, false> : stream_kernel<MAXTILES, false, false>;
+}
+
+StreamKernel stream_kernel_for(int H, bool fused, bool fp4) {
     const int tiles = (H + kStreamCB - 1) / kStreamCB;
-    if (tiles <= 2) return fused ? stream_kernel<2, true> : stream_kernel<2, false>;
-    if (tiles <= 4) return fused ? stream_kernel<4, true> : stream_kernel<4, false>;
-    if (tiles <= 8) return fused ? stream_kernel<8, true> : stream_kernel<8, false>;
+    if (tiles <= 2) return pick<2>(fused, fp4);
+    if (tiles <= 4) return pick<4>(fused, fp4);
+    if (tiles <= 8) return pick<8>(fused, fp4);
     return nullptr;
 }
 
@@ -344,14 +371,14 @@ int stream_smem_bytes(int k, int nstages, bool fused) {
     return ((2 * nstages * 8 + 127) / 128) * 128 + nstages * stream_stage_bytes(k, fused);
 }
 
-cudaError_t stream_prepare(int H, bool fused, int smem_bytes) {
-    StreamKernel kf = stream_kernel_for(H, fused);
+cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes) {
+    StreamKernel kf = stream_kernel_for(H, fused, fp4);
     if (!kf) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    StreamKernel kf = stream_kernel_for(p.H, l.fused != 0);
+    StreamKernel kf = stream_kernel_for(p.H, l.fused != 0, l.fp4 != 0);
     if (!kf) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid_x), 1, 1);

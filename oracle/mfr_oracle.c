@@ -259,6 +259,8 @@ uint8_t mfr_oracle_e4m3_from_f64(double x)
     double a = fabs(x);
     if (a == 0.0)
         return sign;
+    if (isinf(a))                                    /* saturates like any large value */
+        return (uint8_t)(sign | 0x7Eu);
     int e;
     (void)frexp(a, &e);
     int lead = e - 1;

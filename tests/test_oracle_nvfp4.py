@@ -30,6 +30,7 @@ def test_e4m3_rounding_matches_torch_below_saturation(oracle_lib):
 
 def test_e4m3_saturation_and_decoding(oracle_lib):
     for x, b in [(464.0, 0x7E), (480.0, 0x7E), (1e30, 0x7E), (-1e9, 0xFE), (float("nan"), 0x7F),
+                 (float("inf"), 0x7E), (float("-inf"), 0xFE),
                  (0.0, 0x00), (2.0 ** -9, 0x01), (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (448.0, 0x7E)]:
         assert int(oracle_lib.e4m3_from_f64([x])[0]) == b, x
     codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
