@@ -57,6 +57,10 @@ __device__ __forceinline__ void st_f4(float* ptr, float4 v) {
                  :: "l"(ptr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
 }
 
+__device__ __forceinline__ void st_u2(void* ptr, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" :: "l"(ptr), "r"(v.x), "r"(v.y) : "memory");
+}
+
 __device__ __forceinline__ void st_u4(void* ptr, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
                  :: "l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
@@ -174,6 +178,23 @@ __device__ __forceinline__ uint32_t nvfp4_block8(const float (&y)[8], float s_en
 #pragma unroll
     for (int j = 0; j < 4; ++j)
         w |= e2m1x2_rn_sat(__fmul_rn(y[2 * j], enc), __fmul_rn(y[2 * j + 1], enc)) << (8 * j);
+    *sf = s8;
+    return w;
+}
+
+// The same for a 16-element block held by a lane quad (lanes 4m..4m+3, four
+// values each, in column order).  Returns this lane's four codes in 2 bytes.
+__device__ __forceinline__ uint32_t nvfp4_block4(const float (&y)[4], float s_enc, uint32_t* sf) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(y[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    const uint32_t s8 = e4m3_rn_sat(__fmul_rn(__fdiv_rn(amax, 6.0f), s_enc));
+    const float dec = __fdiv_rn(e4m3_to_f32(s8), s_enc);
+    const float enc = (s8 == 0u) ? 0.f : __fdiv_rn(1.0f, dec);
+    const uint32_t w = e2m1x2_rn_sat(__fmul_rn(y[0], enc), __fmul_rn(y[1], enc)) |
+                       (e2m1x2_rn_sat(__fmul_rn(y[2], enc), __fmul_rn(y[3], enc)) << 8);
     *sf = s8;
     return w;
 }

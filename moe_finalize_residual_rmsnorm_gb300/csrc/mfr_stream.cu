@@ -2,10 +2,11 @@
 //
 // One CTA per SM walks a static list of tokens (t = blockIdx.x, += gridDim.x).
 // A producer warp stages, for each token and each column tile of width
-// CB = 8 * NT, the k gathered expert-row segments and the residual segment
+// CB = 2048, the k gathered expert-row segments and the residual segment
 // into a ring of shared-memory stages with bulk asynchronous copies
-// (cp.async.bulk, completion counted in bytes on an mbarrier).  NT consumer
-// threads each own one 16-byte chunk of every tile: they wait for a stage,
+// (cp.async.bulk, completion counted in bytes on an mbarrier).  512 consumer
+// threads (16 warps, so the schedulers always have a warp whose data is in)
+// each own four columns of every tile: they wait for a stage,
 // accumulate acc = fma(w_j, e_j, acc) in slot order, add the residual, write
 // residual_out, release the stage, and keep x in registers; after the last
 // tile of a token they reduce the sum of squares (warp butterfly, then warps
@@ -31,9 +32,10 @@
 namespace mfr {
 namespace {
 
-constexpr int kStreamNT = 256;                 // consumer threads (8 warps)
+constexpr int kColsPT = 4;                     // columns per consumer thread and tile
+constexpr int kStreamNT = 512;                 // consumer threads (16 warps)
 constexpr int kStreamThreads = kStreamNT + 32; // + one producer warp
-constexpr int kStreamCB = kStreamNT * 8;       // columns per tile
+constexpr int kStreamCB = kStreamNT * kColsPT; // columns per tile (2048)
 constexpr int kHeaderBytes = 128;              // per stage: weights + slot mask
 
 struct StageHeader {
@@ -82,46 +84,41 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     __syncthreads();
 
     if (tid >= kStreamNT) {
-        // ================= producer warp (one elected lane) =================
-        if (tid != kStreamNT) return;
+        // ================= producer warp =================
+        // Lane j < k holds slot j of the current token (row index, weight);
+        // lane 0 writes the stage header and arms the stage barrier.  The bulk
+        // copies of a tile issue either from their own lanes at once (lane j
+        // its row, lane kMaxK the residual) or all from lane 0.  Measured on
+        // GB300 at the prefill size: issuing from one lane costs ~0.125 us per
+        // copy, which caps the plain finalize at 4.8 TB/s (224 us) and parallel
+        // issue lifts it to 174 us; the residual + bf16-out form instead runs
+        // 6 % faster from one lane (246 vs 263 us, its writes compete with a
+        // faster read stream), and the NVFP4 form 1.4 % faster in parallel.
+        constexpr bool kParallelIssue = !FUSED || FP4;
         // No explicit launch_dependents: every CTA of this persistent grid runs
         // from start to end, so an early signal would let a dependent grid park
         // its CTAs on every SM for the whole call (measured: a following
         // producer slowed the pair by 17 %).  Dependents launch as CTAs exit.
+        const int lane = tid - kStreamNT;
         int64_t fill = 0;            // stages issued so far
         int s = 0;                   // stage of the next fill
         uint32_t phase = 0;          // how many times the ring wrapped, mod 2
         bool waited = false;
         int64_t t = blockIdx.x;
-        // prefetch the slot indices and weights of the first token
-        int32_t nrow[kMaxK];
-        float nw[kMaxK];
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-            nrow[j] = (j < k && t < p.T) ? p.permuted_row_of[t * k + j] : -1;
-            nw[j] = (j < k && t < p.T) ? p.topk_weights[t * k + j] : 0.f;
-        }
+        // this lane's slot of the first token, loaded ahead
+        int32_t nrow = (lane < k && t < p.T) ? p.permuted_row_of[t * k + lane] : -1;
+        float nw = (lane < k && t < p.T) ? p.topk_weights[t * k + lane] : 0.f;
         bool ok = true;
         for (; t < p.T && ok; t += gridDim.x) {
-            int32_t row[kMaxK];
-            float w[kMaxK];
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j) { row[j] = nrow[j]; w[j] = nw[j]; }
-            const int64_t tn = t + gridDim.x;   // prefetch the next token's slots
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-                nrow[j] = (j < k && tn < p.T) ? p.permuted_row_of[tn * k + j] : -1;
-                nw[j] = (j < k && tn < p.T) ? p.topk_weights[tn * k + j] : 0.f;
-            }
-            uint32_t mask = 0;
-            bool flag = false;
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-                if (j >= k) continue;
-                if (row[j] >= 0 && static_cast<int64_t>(row[j]) < p.R) mask |= 1u << j;
-                else if (!(p.sentinel && row[j] < 0)) flag = true;   // negative = non-local when allowed
-            }
-            if (flag)
+            const int32_t row = nrow;
+            const float w = nw;
+            const int64_t tn = t + gridDim.x;   // load the next token's slot ahead
+            nrow = (lane < k && tn < p.T) ? p.permuted_row_of[tn * k + lane] : -1;
+            nw = (lane < k && tn < p.T) ? p.topk_weights[tn * k + lane] : 0.f;
+            const bool valid = lane < k && row >= 0 && static_cast<int64_t>(row) < p.R;
+            const uint32_t mask = __ballot_sync(0xFFFFFFFFu, valid);          // bit j: slot j
+            const bool bad = lane < k && !valid && !(p.sentinel && row < 0);  // negative = non-local when allowed
+            if (__any_sync(0xFFFFFFFFu, bad) && lane == 0)
                 atomicOr(p.status, MFR_STATUS_BAD_INDEX);
             if (!waited) {
                 pdl_wait();          // expert_out and residual_in come from the previous kernel
@@ -129,53 +126,77 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
             }
             for (int b = 0; b < ntiles; ++b) {
                 // the consumers released the previous fill of this stage
-                if (fill >= nstages && !mbar_wait(smem_u32(&bars[nstages + s]), phase ^ 1u)) {
-                    atomicOr(p.status, MFR_STATUS_TIMEOUT);
-                    s_abort = 1;
+                const bool freed = fill < nstages || mbar_wait(smem_u32(&bars[nstages + s]), phase ^ 1u);
+                if (!__all_sync(0xFFFFFFFFu, freed)) {
+                    if (lane == 0) {
+                        atomicOr(p.status, MFR_STATUS_TIMEOUT);
+                        s_abort = 1;
+                    }
                     ok = false;
                     break;
                 }
                 unsigned char* st = stages + static_cast<size_t>(s) * stage_bytes;
-                StageHeader* hd = reinterpret_cast<StageHeader*>(st);
-#pragma unroll
-                for (int j = 0; j < kMaxK; ++j) hd->w[j] = w[j];
-                hd->mask = mask;
                 const int c0 = b * kStreamCB;
                 const int cb = min(kStreamCB, H - c0);
                 const uint32_t bar = smem_u32(&bars[s]);
-                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask) * cb * 2 + (FUSED ? cb * 4 : 0)));
+                float wl[kMaxK];
 #pragma unroll
-                for (int j = 0; j < kMaxK; ++j)
-                    if (mask & (1u << j))
-                        bulk_g2s(smem_u32(st + kHeaderBytes + j * row_bytes),
-                                 p.expert_out + static_cast<int64_t>(row[j]) * H + c0,
-                                 static_cast<uint32_t>(cb * 2), bar);
-                if (FUSED)
-                    bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
+                for (int j = 0; j < kMaxK; ++j) wl[j] = __shfl_sync(0xFFFFFFFFu, w, j);
+                if (lane == 0) {
+                    StageHeader* hd = reinterpret_cast<StageHeader*>(st);
+#pragma unroll
+                    for (int j = 0; j < kMaxK; ++j) hd->w[j] = wl[j];
+                    hd->mask = mask;
+                    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask) * cb * 2 + (FUSED ? cb * 4 : 0)));
+                }
+                __syncwarp();
+                if constexpr (kParallelIssue) {
+                    if (valid)
+                        bulk_g2s(smem_u32(st + kHeaderBytes + lane * row_bytes),
+                                 p.expert_out + static_cast<int64_t>(row) * H + c0, static_cast<uint32_t>(cb * 2), bar);
+                    if (FUSED && lane == kMaxK)
+                        bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
+                } else {
+                    int32_t rl[kMaxK];
+#pragma unroll
+                    for (int j = 0; j < kMaxK; ++j) rl[j] = __shfl_sync(0xFFFFFFFFu, row, j);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < kMaxK; ++j)
+                            if (mask & (1u << j))
+                                bulk_g2s(smem_u32(st + kHeaderBytes + j * row_bytes),
+                                         p.expert_out + static_cast<int64_t>(rl[j]) * H + c0,
+                                         static_cast<uint32_t>(cb * 2), bar);
+                        bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
+                    }
+                }
                 ++fill;
                 if (++s == nstages) { s = 0; phase ^= 1u; }
             }
         }
-        // drain: every copy this thread issued has landed before the CTA exits
-        for (int64_t f = (fill > nstages ? fill - nstages : 0); f < fill; ++f) {
-            const int sf = static_cast<int>(f % nstages);
-            if (!mbar_wait(smem_u32(&bars[sf]), static_cast<uint32_t>(f / nstages) & 1u)) {
-                atomicOr(p.status, MFR_STATUS_TIMEOUT);
-                break;
+        // drain: every copy this warp issued has landed before the CTA exits
+        if (lane == 0) {
+            for (int64_t f = (fill > nstages ? fill - nstages : 0); f < fill; ++f) {
+                const int sf = static_cast<int>(f % nstages);
+                if (!mbar_wait(smem_u32(&bars[sf]), static_cast<uint32_t>(f / nstages) & 1u)) {
+                    atomicOr(p.status, MFR_STATUS_TIMEOUT);
+                    break;
+                }
             }
         }
         return;
     }
 
     // ===================== consumer threads =====================
+    // Thread tid owns columns [c0 + 4*tid, c0 + 4*tid + 4) of every tile.
     const int warp = tid >> 5;
-    uint32_t g[MAXTILES][4];
+    uint32_t g[MAXTILES][2];
 #pragma unroll
     for (int b = 0; b < MAXTILES; ++b) {
-        const int col = b * kStreamCB + tid * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (FUSED && b < ntiles && col < H) v = *reinterpret_cast<const uint4*>(p.gamma + col);
-        g[b][0] = v.x; g[b][1] = v.y; g[b][2] = v.z; g[b][3] = v.w;
+        const int col = b * kStreamCB + tid * kColsPT;
+        uint2 v = make_uint2(0, 0);
+        if (FUSED && b < ntiles && col < H) v = *reinterpret_cast<const uint2*>(p.gamma + col);
+        g[b][0] = v.x; g[b][1] = v.y;
     }
     pdl_wait();
 
@@ -199,39 +220,33 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 const StageHeader* hd = reinterpret_cast<const StageHeader*>(st);
                 const uint32_t mask = hd->mask;
                 const int c0 = b * kStreamCB;
-                const bool mine = tid * 8 < min(kStreamCB, H - c0);
-                float acc[8];
+                const bool mine = tid * kColsPT < min(kStreamCB, H - c0);
+                float acc[kColsPT];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+                for (int q = 0; q < kColsPT; ++q) acc[q] = 0.f;
                 if (mine) {
 #pragma unroll
                     for (int j = 0; j < kMaxK; ++j) {
                         if (j < k && (mask & (1u << j))) {
                             const float wj = hd->w[j];
-                            const uint4 v = *reinterpret_cast<const uint4*>(st + kHeaderBytes + j * row_bytes + tid * 16);
-                            float e[8];
-                            unpack8(v, e);
+                            const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
+                            const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) acc[q] = __fmaf_rn(wj, e[q], acc[q]);
+                            for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(wj, e[q], acc[q]);
                         }
                     }
                 }
                 __syncwarp();
                 if ((tid & 31) == 0) mbar_arrive(ebar);
-                if (mine) {
-                    uint4 o;
-                    o.x = pack_bf16x2(acc[0], acc[1]);
-                    o.y = pack_bf16x2(acc[2], acc[3]);
-                    o.z = pack_bf16x2(acc[4], acc[5]);
-                    o.w = pack_bf16x2(acc[6], acc[7]);
-                    st_u4(p.out + t * H + c0 + tid * 8, o);
-                }
+                if (mine)
+                    st_u2(p.out + t * H + c0 + tid * kColsPT,
+                          make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3])));
             }
             if (!ok) break;     // warp-uniform: this warp stops; the others time out on their own
         }
     } else {
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
-        float x[MAXTILES][8];
+        float x[MAXTILES][kColsPT];
         float ss = 0.f;
         bool ok = true;
 #pragma unroll
@@ -252,40 +267,34 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
             const uint32_t mask = hd->mask;
             const int c0 = b * kStreamCB;
             const int cb = min(kStreamCB, H - c0);
-            const bool mine = tid * 8 < cb;
-            float acc[8];
+            const bool mine = tid * kColsPT < cb;
+            float acc[kColsPT];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+            for (int q = 0; q < kColsPT; ++q) acc[q] = 0.f;
             if (mine) {
 #pragma unroll
                 for (int j = 0; j < kMaxK; ++j) {
                     if (j < k && (mask & (1u << j))) {
                         const float wj = hd->w[j];
-                        const uint4 v = *reinterpret_cast<const uint4*>(st + kHeaderBytes + j * row_bytes + tid * 16);
-                        float e[8];
-                        unpack8(v, e);
+                        const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
+                        const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) acc[q] = __fmaf_rn(wj, e[q], acc[q]);
+                        for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(wj, e[q], acc[q]);
                     }
                 }
-                const float4 r0 = *reinterpret_cast<const float4*>(st + res_off + tid * 32);
-                const float4 r1 = *reinterpret_cast<const float4*>(st + res_off + tid * 32 + 16);
-                x[b][0] = r0.x + acc[0]; x[b][1] = r0.y + acc[1];
-                x[b][2] = r0.z + acc[2]; x[b][3] = r0.w + acc[3];
-                x[b][4] = r1.x + acc[4]; x[b][5] = r1.y + acc[5];
-                x[b][6] = r1.z + acc[6]; x[b][7] = r1.w + acc[7];
+                const float4 r = *reinterpret_cast<const float4*>(st + res_off + tid * 16);
+                x[b][0] = r.x + acc[0]; x[b][1] = r.y + acc[1];
+                x[b][2] = r.z + acc[2]; x[b][3] = r.w + acc[3];
             } else {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) x[b][q] = 0.f;
+                for (int q = 0; q < kColsPT; ++q) x[b][q] = 0.f;
             }
             __syncwarp();
             if ((tid & 31) == 0) mbar_arrive(ebar);   // this warp is done with the stage
             if (mine) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) ss = __fmaf_rn(x[b][q], x[b][q], ss);
-                float* ro = p.residual_out + t * H + c0 + tid * 8;
-                st_f4(ro, make_float4(x[b][0], x[b][1], x[b][2], x[b][3]));
-                st_f4(ro + 4, make_float4(x[b][4], x[b][5], x[b][6], x[b][7]));
+                for (int q = 0; q < kColsPT; ++q) ss = __fmaf_rn(x[b][q], x[b][q], ss);
+                st_f4(p.residual_out + t * H + c0 + tid * kColsPT, make_float4(x[b][0], x[b][1], x[b][2], x[b][3]));
             }
         }
         ss = warp_allreduce_sum(ss);
@@ -305,38 +314,28 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
         asm volatile("bar.sync 1, %0;" :: "r"(kStreamNT) : "memory");  // s_warp reusable
         if (stop) break;
         const float inv = rsqrtf(tot / static_cast<float>(H) + p.eps);
-        if constexpr (FP4) {
-            // NVFP4: lanes tid and tid^1 hold the two halves of a 16-element block
 #pragma unroll
-            for (int b = 0; b < MAXTILES; ++b) {
-                if (b >= ntiles) break;
-                const int col = b * kStreamCB + tid * 8;
-                float y[8];
+        for (int b = 0; b < MAXTILES; ++b) {
+            if (b >= ntiles) break;
+            const int col = b * kStreamCB + tid * kColsPT;
+            float y[4];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t gw = g[b][q >> 1];
-                    y[q] = (col < H) ? x[b][q] * inv * ((q & 1) ? bf16_hi(gw) : bf16_lo(gw)) : 0.f;
-                }
-                uint32_t sf;
-                const uint32_t w = nvfp4_block8(y, p.s_enc, &sf);
-                if (col < H) {
-                    *reinterpret_cast<uint32_t*>(p.out_q + t * (H / 2) + col / 2) = w;
-                    if ((tid & 1) == 0) p.out_sf[t * (H / 16) + col / 16] = static_cast<uint8_t>(sf);
-                }
+            for (int q = 0; q < kColsPT; ++q) {
+                const uint32_t gw = g[b][q >> 1];
+                y[q] = x[b][q] * inv * ((q & 1) ? bf16_hi(gw) : bf16_lo(gw));
             }
-        } else {
+            if constexpr (FP4) {
+                // NVFP4: the four lanes 4m..4m+3 hold one 16-column block
 #pragma unroll
-            for (int b = 0; b < MAXTILES; ++b) {
-                if (b >= ntiles) break;
-                const int col = b * kStreamCB + tid * 8;
+                for (int q = 0; q < kColsPT; ++q) if (col >= H) y[q] = 0.f;
+                uint32_t sf;
+                const uint32_t w = nvfp4_block4(y, p.s_enc, &sf);
                 if (col < H) {
-                    uint4 o;
-                    o.x = pack_bf16x2(x[b][0] * inv * bf16_lo(g[b][0]), x[b][1] * inv * bf16_hi(g[b][0]));
-                    o.y = pack_bf16x2(x[b][2] * inv * bf16_lo(g[b][1]), x[b][3] * inv * bf16_hi(g[b][1]));
-                    o.z = pack_bf16x2(x[b][4] * inv * bf16_lo(g[b][2]), x[b][5] * inv * bf16_hi(g[b][2]));
-                    o.w = pack_bf16x2(x[b][6] * inv * bf16_lo(g[b][3]), x[b][7] * inv * bf16_hi(g[b][3]));
-                    st_u4(p.out + t * H + col, o);
+                    *reinterpret_cast<uint16_t*>(p.out_q + t * (H / 2) + col / 2) = static_cast<uint16_t>(w);
+                    if ((tid & 3) == 0) p.out_sf[t * (H / 16) + col / 16] = static_cast<uint8_t>(sf);
                 }
+            } else if (col < H) {
+                st_u2(p.out + t * H + col, make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3])));
             }
         }
     }
