@@ -59,3 +59,25 @@ def test_warmup_below_three_is_refused():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.main(["--warmup", "2"]) == 2
+
+
+def test_reference_arm_prints_the_contract_line(capsys, monkeypatch):
+    """bench.py --impl reference times the CPU oracle and prints one JSON line
+    with the keys the benchmark contract asks for."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    rc = bench.main(["--impl", "reference", "--workload", "decode_T8", "--steps", "2", "--warmup", "3",
+                     "--cpu-seconds", "0.05"])
+    assert rc == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 3 and d["gpu_launches"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert "T=8" in d["config"]["workload"]
