@@ -104,6 +104,9 @@ typedef struct mfr_plan_info {
     int smem_bytes;    /* dynamic shared memory per CTA */
     int chunks_per_thread; /* 16-byte column chunks each thread owns per row */
     int sm_count;      /* SMs of the plan's device */
+    int slot_registers; /* CLUSTER / ROWS: 1 = slot rows and weights held in registers
+                           across the dependency wait, 0 = read from shared memory
+                           after it (chosen when the registers would cost a wave) */
 } mfr_plan_info;
 
 typedef struct mfr_plan_s* mfr_plan_t;

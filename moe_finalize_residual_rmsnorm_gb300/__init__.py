@@ -52,7 +52,7 @@ class Options(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("grid_x", ctypes.c_int), ("grid_y", ctypes.c_int),
                 ("block", ctypes.c_int), ("cluster", ctypes.c_int), ("smem_bytes", ctypes.c_int),
-                ("chunks_per_thread", ctypes.c_int), ("sm_count", ctypes.c_int)]
+                ("chunks_per_thread", ctypes.c_int), ("sm_count", ctypes.c_int), ("slot_registers", ctypes.c_int)]
 
     def as_dict(self):
         d = {name: getattr(self, name) for name, _ in self._fields_}

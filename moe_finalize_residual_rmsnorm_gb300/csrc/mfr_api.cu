@@ -212,6 +212,24 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         l.block = round_up((cta_chunks + l.cpt - 1) / l.cpt, 32);
         l.grid_x = static_cast<int>(T > 0 ? T * csize : csize);
         l.smem_bytes = 0;
+        // Slot rows and weights in registers shorten the path from the
+        // dependency wait to the data, unless the extra registers make the
+        // grid take more waves of resident CTAs (512-thread CTAs fit twice
+        // per SM without them, once with them).
+        l.regslots = 1;
+        {
+            int with_regs = 0, without = 0;
+            if ((e = mfr::rows_blocks_per_sm(l, true, &with_regs)) != cudaSuccess ||
+                (e = mfr::rows_blocks_per_sm(l, false, &without)) != cudaSuccess) {
+                cudaGetLastError();
+                return fail_cuda(MFR_ERR_CUDA, "occupancy query", e);
+            }
+            auto waves = [&](int per_sm) -> int64_t {
+                const int64_t slots = static_cast<int64_t>(per_sm) * sms;
+                return slots > 0 ? (l.grid_x + slots - 1) / slots : INT64_MAX;
+            };
+            if (without > 0 && waves(without) < waves(with_regs)) l.regslots = 0;
+        }
         if ((e = mfr::rows_prepare(l)) != cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
@@ -578,6 +596,7 @@ int moe_finalize_rmsnorm_plan_info(mfr_plan_t plan, mfr_plan_info* info) {
     info->smem_bytes = l.smem_bytes;
     info->chunks_per_thread = l.cpt;
     info->sm_count = plan->sm_count;
+    info->slot_registers = l.regslots;
     return MFR_OK;
 }
 

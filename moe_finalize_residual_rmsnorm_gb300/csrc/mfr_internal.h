@@ -43,6 +43,7 @@ struct Launch {
     int fused;        // 1: residual + RMSNorm; 0: plain finalize (out = bf16(sum))
     int fp4;          // 1: the normalised output is written as NVFP4 instead of bf16
     int early_trigger;  // 1: signal dependents at kernel entry (small grids only)
+    int regslots;     // one-CTA-per-token kernels: slot rows/weights held in registers
 };
 
 constexpr int kMaxK = 16;         // slots per token
@@ -55,6 +56,8 @@ void set_last_error(const char* fmt, ...);
 // mfr_rows.cu: one CTA (or one cluster of CTAs) per token.
 bool rows_supported_cpt(int cpt);
 cudaError_t rows_prepare(const Launch& l);   // per-kernel attributes (cluster > 8)
+// Resident CTAs per SM of the kernel l selects, with slot data in registers or not.
+cudaError_t rows_blocks_per_sm(const Launch& l, bool regslots, int* n);
 cudaError_t rows_max_active_clusters(const Launch& l, int* n);
 cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s);
 // An empty kernel with the plan's launch geometry (for the launch floor).

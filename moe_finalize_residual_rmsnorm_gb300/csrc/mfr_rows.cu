@@ -43,8 +43,11 @@ namespace mfr {
 namespace {
 
 // CPT: 16-byte column chunks per thread per row; SG: slots gathered together;
-// FUSED: residual + RMSNorm (true) or plain finalize (false).
-template <int CPT, int SG, bool FUSED, bool FP4>
+// FUSED: residual + RMSNorm (true) or plain finalize (false); RS: each
+// thread holds the slot rows and weights in registers from before the
+// dependency wait (true), or reads them from shared memory as it loads (false:
+// 32 fewer registers, for CTAs whose residency the registers would halve).
+template <int CPT, int SG, bool FUSED, bool FP4, bool RS>
 __global__ void __launch_bounds__(kRowsMaxThreads)
 rows_kernel(const Params p, const int csize)
 {
@@ -103,6 +106,28 @@ rows_kernel(const Params p, const int csize)
     else if (FUSED && tid == kMaxK)
         prefetch_l2_bulk(p.residual_in + t * p.H + col0, static_cast<uint32_t>(nck) * 32u);
 
+    // RS: slot rows and weights go to registers before the wait, so that
+    // after it nothing but address arithmetic stands between the wait and the
+    // loads (measured on decode calls: with the shared-memory reads after the
+    // wait, the time from the wait to the last row doubled).  Threads past
+    // the CTA's chunks load chunk 0 again and discard it, so no load needs a
+    // per-thread branch; an invalid slot (-1) is not loaded at all.
+    int rr[RS ? kMaxK : 1];
+    float ww[RS ? kMaxK : 1];
+    if constexpr (RS) {
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            rr[j] = (j < p.k) ? s_row[j] : -1;
+            ww[j] = (j < p.k) ? s_w[j] : 0.f;
+        }
+    }
+    auto row_of = [&](int j) -> int {
+        if constexpr (RS) return rr[j]; else return (j < p.k) ? s_row[j] : -1;
+    };
+    auto weight_of = [&](int j) -> float {
+        if constexpr (RS) return ww[j]; else return s_w[j];
+    };
+
     pdl_wait();
 
     // ---- residual row and the k expert rows ---------------------------------
@@ -110,10 +135,11 @@ rows_kernel(const Params p, const int csize)
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
         const int c = tid + i * nthreads;
-        if (FUSED && c < nck) {
+        const int cc = c < nck ? c : 0;
+        if (FUSED) {
             const float* res_in = p.residual_in + t * p.H + col0;
-            const float4 a = ld_once_f4(res_in + c * 8);
-            const float4 b = ld_once_f4(res_in + c * 8 + 4);
+            const float4 a = ld_once_f4(res_in + cc * 8);
+            const float4 b = ld_once_f4(res_in + cc * 8 + 4);
             res[i][0] = a.x; res[i][1] = a.y; res[i][2] = a.z; res[i][3] = a.w;
             res[i][4] = b.x; res[i][5] = b.y; res[i][6] = b.z; res[i][7] = b.w;
         } else {
@@ -128,24 +154,28 @@ rows_kernel(const Params p, const int csize)
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[i][q] = 0.f;
 
-    for (int j0 = 0; j0 < p.k; j0 += SG) {
+    // RS: fully unrolled, so rr/ww are indexed by constants and stay in
+    // registers; otherwise a plain loop over the slot groups
+#pragma unroll
+    for (int j0 = 0; j0 < (RS ? kMaxK : p.k); j0 += SG) {
+        if (j0 >= p.k) break;
         uint4 v[SG][CPT];
 #pragma unroll
         for (int s = 0; s < SG; ++s) {
-            const int j = j0 + s;
-            const int r = (j < p.k) ? s_row[j] : -1;
+            const int r = row_of(j0 + s);   // the same for every thread: a uniform branch
             const uint16_t* row = p.expert_out + static_cast<int64_t>(r < 0 ? 0 : r) * p.H + col0;
 #pragma unroll
             for (int i = 0; i < CPT; ++i) {
                 const int c = tid + i * nthreads;
-                v[s][i] = (r >= 0 && c < nck) ? ld_stream_u4(row + c * 8) : make_uint4(0, 0, 0, 0);
+                v[s][i] = make_uint4(0, 0, 0, 0);
+                if (r >= 0) v[s][i] = ld_stream_u4(row + (c < nck ? c : 0) * 8);
             }
         }
 #pragma unroll
         for (int s = 0; s < SG; ++s) {
             const int j = j0 + s;
-            if (j < p.k && s_row[j] >= 0) {
-                const float wj = s_w[j];
+            if (row_of(j) >= 0) {
+                const float wj = weight_of(j);
 #pragma unroll
                 for (int i = 0; i < CPT; ++i) {
                     float e[8];
@@ -259,15 +289,20 @@ rows_kernel(const Params p, const int csize)
 
 using RowsKernel = void (*)(const Params, const int);
 
-RowsKernel rows_kernel_for(int cpt, bool fused, bool fp4) {
-    if (fp4 && !fused) return nullptr;
+template <int CPT, int SG, bool RS>
+RowsKernel pick_rows(bool fused, bool fp4) {
+    if (fp4) return fused ? rows_kernel<CPT, SG, true, true, RS> : nullptr;
+    return fused ? rows_kernel<CPT, SG, true, false, RS> : rows_kernel<CPT, SG, false, false, RS>;
+}
+
+// Shared-memory slot reads (RS = false) are instantiated only for one chunk
+// per thread: the only case where the registers cost residency (512-thread
+// CTAs at 64 vs 112 registers per thread).
+RowsKernel rows_kernel_for(int cpt, bool fused, bool fp4, bool regslots) {
     switch (cpt) {
-        case 1: return fp4 ? rows_kernel<1, 8, true, true>
-                           : (fused ? rows_kernel<1, 8, true, false> : rows_kernel<1, 8, false, false>);
-        case 2: return fp4 ? rows_kernel<2, 8, true, true>
-                           : (fused ? rows_kernel<2, 8, true, false> : rows_kernel<2, 8, false, false>);
-        case 4: return fp4 ? rows_kernel<4, 2, true, true>
-                           : (fused ? rows_kernel<4, 2, true, false> : rows_kernel<4, 2, false, false>);
+        case 1: return regslots ? pick_rows<1, 8, true>(fused, fp4) : pick_rows<1, 8, false>(fused, fp4);
+        case 2: return regslots ? pick_rows<2, 8, true>(fused, fp4) : nullptr;
+        case 4: return regslots ? pick_rows<4, 2, true>(fused, fp4) : nullptr;
         default: return nullptr;
     }
 }
@@ -322,10 +357,16 @@ cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, floor_kernel, status);
 }
 
-bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt, true, false) != nullptr; }
+bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt, true, false, true) != nullptr; }
+
+cudaError_t rows_blocks_per_sm(const Launch& l, bool regslots, int* n) {
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, regslots);
+    if (!k) { *n = 0; return cudaSuccess; }
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k, l.block, static_cast<size_t>(l.smem_bytes));
+}
 
 cudaError_t rows_prepare(const Launch& l) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0);
     if (!k) return cudaErrorInvalidValue;
     if (l.cluster > 8 && l.fused)
         return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -333,7 +374,7 @@ cudaError_t rows_prepare(const Launch& l) {
 }
 
 cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];
@@ -342,7 +383,7 @@ cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
 }
 
 cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];

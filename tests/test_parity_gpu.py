@@ -154,6 +154,23 @@ def test_stream_token_counts_around_the_sm_count(T, H):
     assert plan.info()["variant"] == mfr.VARIANT_STREAM
 
 
+@pytest.mark.parametrize("T", [100, 152, 153, 200, 400])
+def test_rows_kernel_both_slot_forms(T):
+    """The one-CTA-per-token kernel keeps the slot rows and weights in
+    registers across the dependency wait unless that costs a wave of CTAs
+    (512-thread CTAs at H=4096 fit twice per SM without them, once with
+    them); both forms match the oracle, an invalid slot included."""
+    inp = inputs_for(T, 4096, 8, seed=T)
+    idx = inp["permuted_row_of"].clone()
+    idx[T // 2, 3] = -1
+    inp["permuted_row_of"] = idx
+    _, _, _, _, plan = compare_full(inp, dict(variant=mfr.VARIANT_ROWS))
+    info = plan.info()
+    assert info["block"] == 512
+    assert info["slot_registers"] == (1 if T <= info["sm_count"] else 0)
+    assert mfr.Plan(8, 4096, 8, 64).info()["slot_registers"] == 1   # decode cluster
+
+
 def test_variants_agree_bitwise_on_the_residual():
     inp = W.make_inputs(W.PREFILL, "cuda", T=300)
     results = [run_gpu(inp, dict(variant=v, cluster_size=c))
