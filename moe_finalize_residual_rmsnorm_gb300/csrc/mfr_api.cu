@@ -104,6 +104,17 @@ void moe_finalize_rmsnorm_default_options(mfr_options* opt) {
 
 }  // extern "C"
 
+namespace mfr {
+// T = 512 on 152 SMs: 128 CTAs x 4 tokens instead of 56 CTAs with 4 and 96
+// with 3 (measured 4 % faster at H = 8192, and never slower from T = 200 to
+// T = 16384: the last round no longer runs on a fraction of the SMs).
+int stream_grid(int64_t T, int sms) {
+    if (T <= sms) return static_cast<int>(T > 0 ? T : 1);
+    const int64_t rounds = (T + sms - 1) / sms;
+    return static_cast<int>((T + rounds - 1) / rounds);
+}
+}  // namespace mfr
+
 namespace {
 
 // Shared by the fused plan (residual + RMSNorm) and the plain-finalize plan.
@@ -194,7 +205,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         l.block = mfr::stream_threads();
         l.stages = stages;
         l.smem_bytes = mfr::stream_smem_bytes(k, stages, fused);
-        l.grid_x = static_cast<int>(T < sms ? (T > 0 ? T : 1) : sms);
+        l.grid_x = mfr::stream_grid(T, sms);
         // the attribute is per kernel, shared by every plan: always the device
         // maximum, so a plan with a deeper ring never loses its setting
         if ((e = mfr::stream_prepare(static_cast<int>(H), fused, fp4, ring_budget)) != cudaSuccess) {

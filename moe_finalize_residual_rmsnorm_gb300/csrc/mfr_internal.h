@@ -65,6 +65,9 @@ cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s);
 
 // mfr_stream.cu: persistent CTAs fed by bulk copies into a shared-memory ring.
 int stream_threads();
+// Persistent CTAs for T tokens on `sms` SMs: the fewest rounds of one token per
+// CTA, over as few CTAs as give every CTA the same number of tokens (+-1).
+int stream_grid(int64_t T, int sms);
 int stream_stage_bytes(int k, bool fused);
 int stream_smem_bytes(int k, int nstages, bool fused);
 cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes);

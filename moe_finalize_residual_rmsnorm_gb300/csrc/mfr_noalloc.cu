@@ -138,7 +138,7 @@ extern "C" int moe_finalize_rmsnorm_run_noalloc(
 
     mfr::Launch l{};
     l.variant = MFR_VARIANT_STREAM;
-    l.grid_x = static_cast<int>(T < ds.sms ? T : ds.sms);
+    l.grid_x = mfr::stream_grid(T, ds.sms);
     l.grid_y = 1;
     l.block = mfr::stream_threads();
     l.cluster = 1;

@@ -151,7 +151,13 @@ def test_stream_token_counts_around_the_sm_count(T, H):
     tokens than CTAs, ragged last round, ragged last column tile."""
     inp = inputs_for(T, H, 8, seed=T + H)
     _, _, _, _, plan = compare_full(inp, dict(variant=mfr.VARIANT_STREAM))
-    assert plan.info()["variant"] == mfr.VARIANT_STREAM
+    info = plan.info()
+    assert info["variant"] == mfr.VARIANT_STREAM
+    # the fewest rounds of one token per CTA, spread evenly: CTA loads differ by at most one
+    sms = info["sm_count"]
+    rounds = -(-T // sms)
+    assert info["grid_x"] == (T if T <= sms else -(-T // rounds))
+    assert -(-T // info["grid_x"]) == rounds
 
 
 @pytest.mark.parametrize("T", [100, 152, 153, 200, 400])
