@@ -8,7 +8,8 @@ The arithmetic lives in ``mfr_oracle.c`` (plain C, one token and one column at
 a time); this file only builds/loads it and marshals NumPy arrays.  BF16 data
 crosses as ``uint16`` bit patterns.
 
-Pins: every function here is checked in ``tests/test_oracle.py`` against
+Pins: every function here is checked in ``tests/test_oracle.py``,
+``tests/test_oracle_nvfp4.py`` or ``tests/test_oracle_expert_norm.py`` against
 values fixed by the pages or by mathematics (a hand-worked example, closed
 forms, brute force with exact rationals, a library BF16 rounding, a library
 RMSNorm, invariants); ``tests/test_oracle_mutations.py`` shows that planted
@@ -98,6 +99,11 @@ class Oracle:
         lib.mfr_oracle_finalize_residual_rmsnorm_nvfp4.argtypes = [
             i64, i64, i64, i64, p, p, p, p, p, ctypes.c_float, ctypes.c_float, p, p, p, p, i64, p, p]
         lib.mfr_oracle_finalize_residual_rmsnorm_nvfp4.restype = i64
+        lib.mfr_oracle_expert_rmsnorm_f64.argtypes = [i64, i64, i64, i64, p, p, p, p, ctypes.c_float, p, p, i64]
+        lib.mfr_oracle_expert_rmsnorm_f64.restype = i64
+        lib.mfr_oracle_finalize_expert_rmsnorm.argtypes = [
+            i64, i64, i64, i64, p, p, p, p, ctypes.c_float, p, p, i64, p]
+        lib.mfr_oracle_finalize_expert_rmsnorm.restype = i64
         self.lib = lib
         self.path = path
 
@@ -190,6 +196,43 @@ class Oracle:
                                                 _ptr(out), _ptr(tk), n)
         return out, int(bad)
 
+
+    # -- per-expert RMSNorm before the weighted sum (a reading) ---------------
+    def expert_rmsnorm_f64(self, expert_out_bits, permuted_row_of, topk_weights, gamma_bits, eps: float,
+                           tokens: Optional[Sequence[int]] = None):
+        """y = sum_j w[t,j] * RMSNorm(E[idx[t,j]]) * gamma, in double.
+        Returns (y float64 [n, H], number of out-of-range slots)."""
+        E = _c(expert_out_bits, np.uint16)
+        idx = _c(permuted_row_of, np.int32)
+        w = _c(topk_weights, np.float32)
+        g = _c(gamma_bits, np.uint16)
+        R, H = E.shape
+        T, k = idx.shape
+        assert w.shape == (T, k) and g.shape == (H,)
+        tk, n = self._tokens(tokens, T)
+        y = np.empty((n, H), dtype=np.float64)
+        bad = self.lib.mfr_oracle_expert_rmsnorm_f64(T, H, k, R, _ptr(E), _ptr(idx), _ptr(w), _ptr(g),
+                                                     ctypes.c_float(eps), _ptr(y), _ptr(tk), n)
+        return y, int(bad)
+
+    def finalize_expert_rmsnorm(self, expert_out_bits, permuted_row_of, topk_weights, gamma_bits, eps: float,
+                                tokens: Optional[Sequence[int]] = None):
+        """out = BF16(sum_j w[t,j] * RMSNorm(E[idx[t,j]]) * gamma), one
+        rounding from double.  Returns (out uint16 [n, H], bad slots)."""
+        E = _c(expert_out_bits, np.uint16)
+        idx = _c(permuted_row_of, np.int32)
+        w = _c(topk_weights, np.float32)
+        g = _c(gamma_bits, np.uint16)
+        R, H = E.shape
+        T, k = idx.shape
+        assert w.shape == (T, k) and g.shape == (H,)
+        tk, n = self._tokens(tokens, T)
+        out = np.empty((n, H), dtype=np.uint16)
+        scratch = np.empty(H, dtype=np.float64)
+        bad = self.lib.mfr_oracle_finalize_expert_rmsnorm(T, H, k, R, _ptr(E), _ptr(idx), _ptr(w), _ptr(g),
+                                                          ctypes.c_float(eps), _ptr(out), _ptr(tk), n,
+                                                          _ptr(scratch))
+        return out, int(bad)
 
     # -- NVFP4 ----------------------------------------------------------------
     def e4m3_from_f64(self, x) -> np.ndarray:

@@ -35,6 +35,9 @@
  * eps inside the square root; y = x / rms * gamma (not 1 + gamma); an index
  * outside [0, R) makes its slot contribute nothing and is counted.
  *
+ * A second reading of [C] section 2.1 (an RMSNorm per expert row before the
+ * weighted sum, no residual) is kept apart at the end of the file.
+ *
  * Precision: steps [A] and the residual add are FP32, exactly as the pages fix
  * them.  The normalisation is not fixed by the pages, so the oracle computes
  * it in double and rounds once, from double, to BF16 (nearest, ties to even).
@@ -225,6 +228,74 @@ int64_t mfr_oracle_finalize_only(int64_t T, int64_t H, int64_t k, int64_t R,
             }
             out[i * H + h] = mfr_oracle_bf16_from_f64((double)acc);
         }
+    }
+    return bad;
+}
+
+/* ---- per-expert RMSNorm before the weighted sum (a reading) ----------------
+ *
+ * [C] section 2.1 names a TP finalize that fuses the TP reduction, an RMSNorm
+ * per expert and the weighted accumulation, straight from the GEMM2 result,
+ * and gives no formula.  On one GPU the TP reduction is the identity; the
+ * plainest reading is taken: each gathered expert row is RMS-normalised over
+ * its own H columns with the shared gamma, and the normalised rows are summed
+ * with the router weights.  No residual.
+ *     n_j[h]    = E[r_j, h] / sqrt(mean_h(E[r_j, :]^2) + eps) * gamma[h]
+ *     y[t, h]   = sum_j w[t, j] * n_j[h]            (slots j = 0..k-1 as stored)
+ *     out[t, h] = BF16(y[t, h])
+ * Everything in double, one rounding to BF16; a slot whose index lies outside
+ * [0, R) contributes nothing and is counted.
+ */
+
+/* y (double [n, H]) of the tokens asked for; returns the bad-slot count. */
+int64_t mfr_oracle_expert_rmsnorm_f64(int64_t T, int64_t H, int64_t k, int64_t R,
+                                      const uint16_t* expert_out, const int32_t* idx,
+                                      const float* w, const uint16_t* gamma, float eps,
+                                      double* y, const int64_t* tokens, int64_t ntokens)
+{
+    int64_t bad = 0;
+    int64_t n = tokens ? ntokens : T;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        double* yr = y + i * H;
+        bad += count_bad_slots(t, k, R, idx);
+        for (int64_t h = 0; h < H; ++h)
+            yr[h] = 0.0;
+        for (int64_t j = 0; j < k; ++j) {
+            int32_t r = idx[t * k + j];
+            if (!slot_valid(r, R))
+                continue;
+            const uint16_t* row = expert_out + (int64_t)r * H;
+            double ss = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+                double e = mfr_oracle_bf16_to_f64(row[h]);
+                ss += e * e;
+            }
+            double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
+            double wj = (double)w[t * k + j];
+            for (int64_t h = 0; h < H; ++h)
+                yr[h] += wj * (mfr_oracle_bf16_to_f64(row[h]) * inv * mfr_oracle_bf16_to_f64(gamma[h]));
+        }
+    }
+    return bad;
+}
+
+/* out = BF16(y) for the tokens asked for, one token at a time through an
+ * H-double scratch row. */
+int64_t mfr_oracle_finalize_expert_rmsnorm(int64_t T, int64_t H, int64_t k, int64_t R,
+                                           const uint16_t* expert_out, const int32_t* idx,
+                                           const float* w, const uint16_t* gamma, float eps,
+                                           uint16_t* out, const int64_t* tokens, int64_t ntokens,
+                                           double* y_scratch)
+{
+    int64_t bad = 0;
+    int64_t n = tokens ? ntokens : T;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        bad += mfr_oracle_expert_rmsnorm_f64(T, H, k, R, expert_out, idx, w, gamma, eps,
+                                             y_scratch, &t, 1);
+        for (int64_t h = 0; h < H; ++h)
+            out[i * H + h] = mfr_oracle_bf16_from_f64(y_scratch[h]);
     }
     return bad;
 }

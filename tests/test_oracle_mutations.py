@@ -3,7 +3,8 @@
 Each case copies the oracle's C source, plants one plausible mistake (a
 dropped term, a wrong sign, a wrong index, a misplaced eps, a wrong rounding,
 a reversed slot order ...), compiles the copy on the CPU, and runs every pin
-of tests/test_oracle.py and tests/test_oracle_nvfp4.py against it.  At least one pin must fail.  The real
+of tests/test_oracle.py, tests/test_oracle_nvfp4.py and
+tests/test_oracle_expert_norm.py against it.  At least one pin must fail.  The real
 oracle is never modified.
 """
 import importlib.util
@@ -70,6 +71,20 @@ MUTATIONS = {
                            "            float sv = v;")],
     "amax_over_8": [("            for (int j = 0; j < 16; ++j)\n                if (fabsf(yb[j]) > amax)",
                      "            for (int j = 0; j < 8; ++j)\n                if (fabsf(yb[j]) > amax)")],
+    "expert_norm_gamma_dropped": [
+        ("yr[h] += wj * (mfr_oracle_bf16_to_f64(row[h]) * inv * mfr_oracle_bf16_to_f64(gamma[h]));",
+         "yr[h] += wj * (mfr_oracle_bf16_to_f64(row[h]) * inv);")],
+    "expert_norm_weights_ignored": [("double wj = (double)w[t * k + j];", "double wj = 1.0;")],
+    "expert_norm_mean_over_k": [("ss / (double)H + (double)eps);\n            double wj",
+                                 "ss / (double)k + (double)eps);\n            double wj")],
+    "expert_norm_squares_carried_across_slots": [
+        ("            const uint16_t* row = expert_out + (int64_t)r * H;\n            double ss = 0.0;\n",
+         "            const uint16_t* row = expert_out + (int64_t)r * H;\n"),
+        ("        for (int64_t j = 0; j < k; ++j) {\n            int32_t r = idx[t * k + j];\n            if (!slot_valid(r, R))\n                continue;\n            const uint16_t* row",
+         "        double ss = 0.0;\n        for (int64_t j = 0; j < k; ++j) {\n            int32_t r = idx[t * k + j];\n            if (!slot_valid(r, R))\n                continue;\n            const uint16_t* row")],
+    "expert_norm_bad_slot_reads_row_0": [
+        ("            if (!slot_valid(r, R))\n                continue;\n            const uint16_t* row",
+         "            if (!slot_valid(r, R))\n                r = 0;\n            const uint16_t* row")],
     "finalize_only_double_rounding": [
         ("out[i * H + h] = mfr_oracle_bf16_from_f64((double)acc);",
          "out[i * H + h] = mfr_oracle_bf16_from_f64((double)(acc * 1.0009765625f));")],
@@ -78,7 +93,7 @@ MUTATIONS = {
 
 def _load_pins():
     runs = []
-    for fname in ("test_oracle.py", "test_oracle_nvfp4.py"):
+    for fname in ("test_oracle.py", "test_oracle_nvfp4.py", "test_oracle_expert_norm.py"):
         runs += _pins_of(fname)
     return runs
 
