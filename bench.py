@@ -484,17 +484,19 @@ def run_sweep(mfr, device, args):
 
 
 def run_variants(mfr, device, wl, sets, args):
-    """The other two outputs of the library on the headline workload, timed
+    """The other outputs of the library on the headline workload, timed
     like the main step (two alternating input sets, CUDA events):
     plain finalize (bf16 sum, no residual or norm: k*H*2 + H*2 + k*8 bytes
-    per token) and the NVFP4 epilogue (residual + RMSNorm, output as E2M1
-    codes + E4M3 block scales: k*H*2 + H*8 + H/2 + H/16 + k*8 bytes)."""
+    per token), the NVFP4 epilogue (residual + RMSNorm, output as E2M1
+    codes + E4M3 block scales: k*H*2 + H*8 + H/2 + H/16 + k*8 bytes) and the
+    finalize with an RMSNorm per expert row (k*H*2 + H*2 + k*8 bytes)."""
     T, H, k, R = wl.T, wl.H, wl.k, wl.R
     steps = max(20, min(args.steps, 500))
     stream = torch.cuda.Stream(device)
     out = {}
     fin = mfr.FinalizePlan(T, H, k, R, enable_pdl=not args.no_pdl)
     fp4 = mfr.Nvfp4Plan(T, H, k, R, enable_pdl=not args.no_pdl)
+    en = mfr.ExpertNormPlan(T, H, k, R, enable_pdl=not args.no_pdl)
     q = [torch.empty((T, H // 2), dtype=torch.uint8, device=device) for _ in range(2)]
     sf = [torch.empty((T, H // 16), dtype=torch.uint8, device=device) for _ in range(2)]
     s_enc = 448.0 * 6.0 / 16.0
@@ -508,8 +510,15 @@ def run_variants(mfr, device, wl, sets, args):
         fp4.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["residual"], d["residual_out"],
                 d["gamma"], d["eps"], s_enc, q[i & 1], sf[i & 1], stream, validate=False)
 
+    def en_step(i):
+        d = sets[i & 1]
+        en.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["gamma"], d["eps"], d["out"], stream,
+               validate=False)
+
+    plans = {"finalize_only": fin, "nvfp4_epilogue": fp4, "expert_rmsnorm": en}
     for name, fn, nbytes in (("finalize_only", fin_step, T * (k * H * 2 + H * 2 + k * 8)),
-                             ("nvfp4_epilogue", fp4_step, T * (k * H * 2 + H * 8 + H // 2 + H // 16 + k * 8))):
+                             ("nvfp4_epilogue", fp4_step, T * (k * H * 2 + H * 8 + H // 2 + H // 16 + k * 8)),
+                             ("expert_rmsnorm", en_step, T * (k * H * 2 + H * 2 + k * 8))):
         for i in range(5):
             fn(i)
         stream.synchronize()
@@ -522,8 +531,8 @@ def run_variants(mfr, device, wl, sets, args):
         us = a.elapsed_time(b) * 1e3 / steps
         out[name] = {"us_per_call": round(us, 2), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                      "bytes_per_call": int(nbytes), "steps": steps,
-                     "variant": (fin if name == "finalize_only" else fp4).info()["variant_name"]}
-    if fin.get_status(stream) or fp4.get_status(stream):
+                     "variant": plans[name].info()["variant_name"]}
+    if fin.get_status(stream) or fp4.get_status(stream) or en.get_status(stream):
         raise RuntimeError("status word set while timing the variants")
     return out
 

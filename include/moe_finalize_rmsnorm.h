@@ -233,6 +233,33 @@ int moe_finalize_rmsnorm_plan_info(mfr_plan_t plan, mfr_plan_info* info);
  * sure no run of this plan is still in flight. */
 void moe_finalize_rmsnorm_destroy(mfr_plan_t plan);
 
+/* ---- finalize with an RMSNorm per expert row (a reading) ----------------
+ * The PR 6544 analysis ("FlashInfer, Muse-Spark-Open을 위한 융합 정규화 및
+ * TP/EP MoE 최적화로 성능 극대화", section 2.1) names a tensor-parallel MoE
+ * finalize that fuses the TP reduction, an RMSNorm per expert and the
+ * weighted accumulation, and gives no formula.  On one GPU the TP reduction
+ * is the identity; this entry point computes the plainest reading:
+ *     inv_j     = rsqrt(mean_h(E[r_j, :]^2) + eps)          (FP32, per row)
+ *     out[t, h] = bf16( sum_j w[t,j] * ((E[r_j, h] * inv_j) * gamma[h]) )
+ * with r_j = permuted_row_of[t, j], FP32 fused multiply-adds in slot order
+ * j = 0..k-1, the shared gamma, and no residual.  One CTA per token
+ * (MFR_VARIANT_ROWS; AUTO picks it, CLUSTER and STREAM are refused).
+ *
+ * moe_finalize_expert_rmsnorm_plan: as moe_finalize_rmsnorm_plan (same
+ * shape rules and options; cluster_size is ignored).
+ * moe_finalize_expert_rmsnorm_run: expert_out bf16 [R, H], permuted_row_of
+ * int32 [T, k], topk_weights fp32 [T, k], gamma bf16 [H], out bf16 [T, H];
+ * device pointers, 16-byte aligned (4 for the index map and weights); out
+ * must not overlap an input; eps finite and >= 0.  Slot index rules, the
+ * status word, debug_checks and sentinel_skip as for moe_finalize_rmsnorm_run.
+ * Asynchronous; returns MFR_OK or an MFR_ERR_* code.  _get_status,
+ * _plan_info, _launch_floor and _destroy take this plan too. */
+int moe_finalize_expert_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                                     const mfr_options* opt);
+int moe_finalize_expert_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
+                                    const float* topk_weights, const void* gamma, float eps, void* out,
+                                    void* stream);
+
 /* ---- benchmarking stand-in for the producer of expert_out ---------------
  * Enqueues a kernel that follows the protocol the PR 5319 analysis (section
  * 2) gives the FC2 grouped GEMM: wait for the previous kernel, immediately

@@ -19,7 +19,7 @@ from typing import Optional
 from .build import LIBRARY, build as _build_library
 
 __all__ = [
-    "LIBRARY", "MFRError", "Plan", "FinalizePlan", "Nvfp4Plan", "PlanInfo", "Options", "build", "load_library", "supports",
+    "LIBRARY", "MFRError", "Plan", "FinalizePlan", "Nvfp4Plan", "ExpertNormPlan", "PlanInfo", "Options", "build", "load_library", "supports",
     "moe_finalize_residual_rmsnorm", "finalize_residual_rmsnorm_host", "exported_symbols",
     "VARIANT_AUTO", "VARIANT_CLUSTER", "VARIANT_ROWS", "VARIANT_STREAM", "STATUS_BAD_INDEX",
     "ERROR_CODES",
@@ -77,6 +77,8 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_nvfp4_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _F, _F, _VP, _VP, _VP]),
     "moe_finalize_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
     "moe_finalize_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
+    "moe_finalize_expert_rmsnorm_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
+    "moe_finalize_expert_rmsnorm_run": (_I, [_VP, _VP, _VP, _VP, _VP, _F, _VP, _VP]),
     "moe_finalize_rmsnorm_run_noalloc": (_I, [_I64, _I64, _I, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _I,
                                                ctypes.POINTER(_I), _VP]),
     "moe_finalize_rmsnorm_destroy": (None, [_VP]),
@@ -305,6 +307,30 @@ class FinalizePlan(Plan):
         code = self._lib.moe_finalize_run(self._h, _ptr(expert_out), _ptr(permuted_row_of), _ptr(topk_weights),
                                           _ptr(out), _stream_handle(stream))
         _check(code, "moe_finalize_run")
+
+
+class ExpertNormPlan(Plan):
+    """Finalize with an RMSNorm per expert row before the weighted sum:
+    out = bf16(sum_j w_j * ((E[r_j] * rsqrt(mean(E[r_j]^2) + eps)) * gamma)),
+    no residual (C: moe_finalize_expert_rmsnorm_plan / _run)."""
+
+    _PLAN_FN = "moe_finalize_expert_rmsnorm_plan"
+
+    def run(self, expert_out, permuted_row_of, topk_weights, gamma, eps: float, out, stream=None, *,
+            validate: bool = True):
+        if validate:
+            import torch
+            for name, t, dt, shape in [("expert_out", expert_out, torch.bfloat16, (self.R, self.H)),
+                                       ("permuted_row_of", permuted_row_of, torch.int32, (self.T, self.k)),
+                                       ("topk_weights", topk_weights, torch.float32, (self.T, self.k)),
+                                       ("gamma", gamma, torch.bfloat16, (self.H,)),
+                                       ("out", out, torch.bfloat16, (self.T, self.H))]:
+                if t.dtype != dt or tuple(t.shape) != shape or not t.is_cuda or not t.is_contiguous():
+                    raise ValueError(f"{name}: expected contiguous CUDA {dt} {shape}")
+        code = self._lib.moe_finalize_expert_rmsnorm_run(self._h, _ptr(expert_out), _ptr(permuted_row_of),
+                                                         _ptr(topk_weights), _ptr(gamma), ctypes.c_float(eps),
+                                                         _ptr(out), _stream_handle(stream))
+        _check(code, "moe_finalize_expert_rmsnorm_run")
 
 
 def bench_producer(src, expert_out, busy_cycles: int = 0, enable_pdl: bool = True, stream=None) -> None:

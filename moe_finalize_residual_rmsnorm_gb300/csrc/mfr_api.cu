@@ -23,6 +23,7 @@ struct mfr_plan_s {
     int* d_status;
     bool fused;        // residual + RMSNorm (false: moe_finalize_plan's plain finalize)
     bool fp4;          // made by moe_finalize_rmsnorm_nvfp4_plan: NVFP4 output
+    bool expert_norm;  // made by moe_finalize_expert_rmsnorm_plan
 };
 
 namespace {
@@ -119,7 +120,7 @@ namespace {
 
 // Shared by the fused plan (residual + RMSNorm) and the plain-finalize plan.
 int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mfr_options* opt,
-              bool fused, bool fp4) {
+              bool fused, bool fp4, bool expert_norm = false) {
     g_last_error[0] = '\0';
     if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
     *plan = nullptr;
@@ -172,6 +173,19 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     const int ring_budget = smem_optin - 1024;                // static shared memory and slack
     int stages = 0;
     while (stages < kMaxStages && mfr::stream_smem_bytes(k, stages + 1, fused) <= ring_budget) ++stages;
+    if (expert_norm) {
+        // one CTA per token (mfr_expert_norm.cu), or the ring kernel, which
+        // keeps each thread's share of the token's rows in registers: k <= 8
+        // and at most 4 column tiles (H <= 8192)
+        const bool ring_ok = k <= 8 && H <= 8192 && stages >= 2;
+        if (variant == MFR_VARIANT_CLUSTER)
+            return fail(MFR_ERR_INVALID_ARG, "the per-expert RMSNorm finalize has no cluster variant");
+        if (variant == MFR_VARIANT_STREAM && !ring_ok)
+            return fail(MFR_ERR_UNSUPPORTED_SHAPE, "the per-expert RMSNorm ring kernel needs k <= 8 and H <= 8192");
+        if (variant == MFR_VARIANT_AUTO)
+            variant = (ring_ok && T * H >= kRowsMaxElems) ? MFR_VARIANT_STREAM : MFR_VARIANT_ROWS;
+        csize = 1;
+    }
     if (variant == MFR_VARIANT_AUTO) {
         const int64_t elems = T * H;
         if (elems <= kClusterMaxElems) {
@@ -191,6 +205,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     while (fp4 && csize > 1 && (chunks / csize) % 2 != 0) csize /= 2;
     if (variant == MFR_VARIANT_CLUSTER && csize < 2) variant = MFR_VARIANT_ROWS;
     l.variant = variant;
+    l.expert_norm = expert_norm ? 1 : 0;
     // Signal dependents at kernel entry only while this grid is small: a
     // large grid would let the next kernel park CTAs on every SM for the
     // whole call (the ring kernel never signals early, see mfr_stream.cu).
@@ -208,7 +223,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         l.grid_x = mfr::stream_grid(T, sms);
         // the attribute is per kernel, shared by every plan: always the device
         // maximum, so a plan with a deeper ring never loses its setting
-        if ((e = mfr::stream_prepare(static_cast<int>(H), fused, fp4, ring_budget)) != cudaSuccess) {
+        if ((e = mfr::stream_prepare(static_cast<int>(H), fused, fp4, ring_budget, expert_norm)) != cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }
@@ -228,7 +243,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         // grid take more waves of resident CTAs (512-thread CTAs fit twice
         // per SM without them, once with them).
         l.regslots = 1;
-        {
+        if (!expert_norm) {   // that kernel always holds them in registers
             int with_regs = 0, without = 0;
             if ((e = mfr::rows_blocks_per_sm(l, true, &with_regs)) != cudaSuccess ||
                 (e = mfr::rows_blocks_per_sm(l, false, &without)) != cudaSuccess) {
@@ -241,7 +256,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
             };
             if (without > 0 && waves(without) < waves(with_regs)) l.regslots = 0;
         }
-        if ((e = mfr::rows_prepare(l)) != cudaSuccess) {
+        if (!expert_norm && (e = mfr::rows_prepare(l)) != cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }
@@ -282,6 +297,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     p->d_status = status;
     p->fused = fused;
     p->fp4 = fp4;
+    p->expert_norm = expert_norm;
     *plan = p;
     return MFR_OK;
 }
@@ -304,11 +320,79 @@ int moe_finalize_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, 
     return make_plan(plan, T, H, k, R, opt, false, false);
 }
 
+int moe_finalize_expert_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                                     const mfr_options* opt) {
+    return make_plan(plan, T, H, k, R, opt, false, false, true);
+}
+
+int moe_finalize_expert_rmsnorm_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
+                                    const float* topk_weights, const void* gamma, float eps, void* out,
+                                    void* stream) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    if (!plan->expert_norm)
+        return fail(MFR_ERR_INVALID_ARG, "this plan was not made by moe_finalize_expert_rmsnorm_plan");
+    const int64_t T = plan->T, H = plan->H, R = plan->R;
+    const int k = plan->k;
+    if (T == 0) return MFR_OK;
+    if (!permuted_row_of || !topk_weights || !gamma || !out || (R > 0 && !expert_out))
+        return fail(MFR_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!std::isfinite(eps) || eps < 0.f)
+        return fail(MFR_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (!aligned(expert_out, 16) || !aligned(gamma, 16) || !aligned(out, 16))
+        return fail(MFR_ERR_MISALIGNED, "expert_out, gamma and out must be 16-byte aligned");
+    if (!aligned(permuted_row_of, 4) || !aligned(topk_weights, 4))
+        return fail(MFR_ERR_MISALIGNED, "permuted_row_of and topk_weights must be 4-byte aligned");
+    const size_t n_out = static_cast<size_t>(T * H) * 2;
+    const size_t n_e = static_cast<size_t>(R * H) * 2;
+    const size_t n_tk = static_cast<size_t>(T * k) * 4;
+    if (overlaps(out, n_out, expert_out, n_e) || overlaps(out, n_out, permuted_row_of, n_tk) ||
+        overlaps(out, n_out, topk_weights, n_tk) || overlaps(out, n_out, gamma, static_cast<size_t>(H) * 2))
+        return fail(MFR_ERR_INVALID_ARG, "out overlaps an input");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { cudaGetLastError(); return fail_cuda(MFR_ERR_CUDA, "cudaGetDevice", e); }
+    if (dev != plan->device)
+        return fail(MFR_ERR_INVALID_ARG, "current device %d is not the plan's device %d", dev, plan->device);
+
+    mfr::Params p{};
+    p.expert_out = static_cast<const uint16_t*>(expert_out);
+    p.permuted_row_of = permuted_row_of;
+    p.topk_weights = topk_weights;
+    p.gamma = static_cast<const uint16_t*>(gamma);
+    p.out = static_cast<uint16_t*>(out);
+    p.status = plan->d_status;
+    p.T = T;
+    p.R = R;
+    p.H = static_cast<int>(H);
+    p.k = k;
+    p.eps = eps;
+    p.sentinel = plan->opt.sentinel_skip ? 1 : 0;
+    p.early_trigger = plan->launch.early_trigger;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = plan->launch.variant == MFR_VARIANT_STREAM ? mfr::stream_launch(p, plan->launch, s)
+                                                   : mfr::expert_norm_launch(p, plan->launch, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_LAUNCH, "kernel launch", e);
+    }
+    if (plan->opt.debug_checks) {
+        int st = 0;
+        const int rc = moe_finalize_rmsnorm_get_status(plan, stream, &st);
+        if (rc != MFR_OK) return rc;
+        if (st & MFR_STATUS_BAD_INDEX)
+            return fail(MFR_ERR_BAD_INDEX, "a permuted_row_of entry was outside [0, %lld)", (long long)R);
+    }
+    return MFR_OK;
+}
+
 int moe_finalize_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_row_of,
                      const float* topk_weights, void* out, void* stream) {
     g_last_error[0] = '\0';
     if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
     if (plan->fused) return fail(MFR_ERR_INVALID_ARG, "this plan was made by moe_finalize_rmsnorm_plan");
+    if (plan->expert_norm)
+        return fail(MFR_ERR_INVALID_ARG, "this plan was made by moe_finalize_expert_rmsnorm_plan");
     const int64_t T = plan->T, H = plan->H, R = plan->R;
     const int k = plan->k;
     if (T == 0) return MFR_OK;

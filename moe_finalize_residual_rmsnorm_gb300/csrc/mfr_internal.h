@@ -44,6 +44,7 @@ struct Launch {
     int fp4;          // 1: the normalised output is written as NVFP4 instead of bf16
     int early_trigger;  // 1: signal dependents at kernel entry (small grids only)
     int regslots;     // one-CTA-per-token kernels: slot rows/weights held in registers
+    int expert_norm;  // 1: RMSNorm per expert row before the weighted sum (mfr_expert_norm.cu)
 };
 
 constexpr int kMaxK = 16;         // slots per token
@@ -63,6 +64,10 @@ cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s);
 // An empty kernel with the plan's launch geometry (for the launch floor).
 cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s);
 
+// mfr_expert_norm.cu: one CTA per token, each expert row RMS-normalised
+// before the weighted sum.  Launch uses grid_x (tokens), block, cpt, pdl.
+cudaError_t expert_norm_launch(const Params& p, const Launch& l, cudaStream_t s);
+
 // mfr_stream.cu: persistent CTAs fed by bulk copies into a shared-memory ring.
 int stream_threads();
 // Persistent CTAs for T tokens on `sms` SMs: the fewest rounds of one token per
@@ -70,7 +75,7 @@ int stream_threads();
 int stream_grid(int64_t T, int sms);
 int stream_stage_bytes(int k, bool fused);
 int stream_smem_bytes(int k, int nstages, bool fused);
-cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes);
+cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en = false);
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s);
 
 }  // namespace mfr

@@ -15,6 +15,14 @@
 // With FUSED = false it is the plain finalize of the PR 5319 page: no
 // residual in the stages, out = bf16(acc) written tile by tile, no norm.
 //
+// With EN = true (FUSED = false, k <= 8, at most 4 tiles) it is the finalize
+// with an RMSNorm per expert row, the reading of the PR 6544 analysis, section
+// 2.1 (see mfr_expert_norm.cu): each consumer thread keeps its four columns
+// of every slot and tile packed in registers while it sums each slot's
+// squares, the CTA reduces the k sums (warp butterfly, then warps in index
+// order), c_j = w_j * rsqrt(ss_j / H + eps), and out = bf16(gamma *
+// sum_j c_j * e_j) with FMAs in slot order.  The stages carry only the rows.
+//
 // The ring keeps several tiles in flight per SM at all times, so the gather
 // never drains between tokens (the register-gather kernel stalls on each
 // token's index load and block barrier).  Operation and citations are those
@@ -53,8 +61,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 }
 
 // MAXTILES: upper bound on ceil(H / CB) for this instantiation;
-// FUSED: residual + RMSNorm (true) or plain finalize (false).
-template <int MAXTILES, bool FUSED, bool FP4>
+// FUSED: residual + RMSNorm (true) or plain finalize (false); EN: per-expert
+// RMSNorm (with FUSED = false).
+template <int MAXTILES, bool FUSED, bool FP4, bool EN>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 stream_kernel(const Params p, const int nstages, const int stage_bytes)
 {
@@ -64,6 +73,8 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     unsigned char* stages = smem + ((2 * nstages * 8 + 127) / 128) * 128;
     __shared__ float s_warp[kStreamNT / 32];
+    __shared__ float s_slot[EN ? kStreamNT / 32 : 1][EN ? 8 : 1];   // EN: per-warp slot sums
+    __shared__ float s_coef[EN ? 8 : 1];                            // EN: c_j of the token
     __shared__ int s_abort;
 
     const int tid = threadIdx.x;
@@ -195,14 +206,107 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     for (int b = 0; b < MAXTILES; ++b) {
         const int col = b * kStreamCB + tid * kColsPT;
         uint2 v = make_uint2(0, 0);
-        if (FUSED && b < ntiles && col < H) v = *reinterpret_cast<const uint2*>(p.gamma + col);
+        if ((FUSED || EN) && b < ntiles && col < H) v = *reinterpret_cast<const uint2*>(p.gamma + col);
         g[b][0] = v.x; g[b][1] = v.y;
     }
     pdl_wait();
 
     int s = 0;
     uint32_t phase = 0;
-    if constexpr (!FUSED) {
+    if constexpr (EN) {
+        // ---- RMSNorm per expert row: rows kept packed until the token's c_j are known
+        const int lane = tid & 31;
+        for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
+            uint2 rv[MAXTILES][8];
+            float ss[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ss[j] = 0.f;
+            uint32_t mask = 0;
+            float my_w = 0.f;       // thread j < k: the weight of slot j
+            bool ok = true;
+#pragma unroll
+            for (int b = 0; b < MAXTILES; ++b) {
+                if (b >= ntiles) break;
+                const uint32_t bar = smem_u32(&bars[s]);
+                const uint32_t ebar = smem_u32(&bars[nstages + s]);
+                const unsigned char* st = stages + static_cast<size_t>(s) * stage_bytes;
+                const bool landed = __all_sync(0xFFFFFFFFu, mbar_wait(bar, phase));
+                if (++s == nstages) { s = 0; phase ^= 1u; }
+                if (!landed) {
+                    atomicOr(p.status, MFR_STATUS_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                const StageHeader* hd = reinterpret_cast<const StageHeader*>(st);
+                mask = hd->mask;
+                if (tid < 8) my_w = hd->w[tid];
+                const int c0 = b * kStreamCB;
+                const bool mine = tid * kColsPT < min(kStreamCB, H - c0);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    rv[b][j] = make_uint2(0, 0);
+                    if (j < k && (mask & (1u << j)) && mine) {
+                        const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
+                        rv[b][j] = v;
+                        const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+#pragma unroll
+                        for (int q = 0; q < kColsPT; ++q) ss[j] = __fmaf_rn(e[q], e[q], ss[j]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ebar);     // this warp is done with the stage
+            }
+            // per-slot sums over the CTA: warp butterfly, then warps in index order
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float v = warp_allreduce_sum(ss[j]);
+                if (lane == 0) s_slot[warp][j] = v;
+            }
+            const uint32_t stop_in = (!ok || s_abort != 0) ? 1u : 0u;
+            uint32_t stop;
+            asm volatile("{\n\t.reg .pred pin, pout;\n\t"
+                         "setp.ne.u32 pin, %1, 0;\n\t"
+                         "bar.red.or.pred pout, 1, %2, pin;\n\t"
+                         "selp.u32 %0, 1, 0, pout;\n\t}"
+                         : "=r"(stop) : "r"(stop_in), "r"(kStreamNT) : "memory");
+            if (stop) break;
+            if (tid < k) {
+                float tot = 0.f;
+#pragma unroll
+                for (int w = 0; w < kStreamNT / 32; ++w) tot += s_slot[w][tid];
+                s_coef[tid] = my_w * rsqrtf(tot / static_cast<float>(H) + p.eps);
+            }
+            asm volatile("bar.sync 1, %0;" :: "r"(kStreamNT) : "memory");   // s_coef ready, s_slot reusable
+            float cj[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cj[j] = (j < k) ? s_coef[j] : 0.f;
+#pragma unroll
+            for (int b = 0; b < MAXTILES; ++b) {
+                if (b >= ntiles) break;
+                const int col = b * kStreamCB + tid * kColsPT;
+                if (col >= H) continue;
+                float acc[kColsPT];
+#pragma unroll
+                for (int q = 0; q < kColsPT; ++q) acc[q] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j < k && (mask & (1u << j))) {
+                        const uint2 v = rv[b][j];
+                        const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+#pragma unroll
+                        for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(cj[j], e[q], acc[q]);
+                    }
+                }
+                float y[kColsPT];
+#pragma unroll
+                for (int q = 0; q < kColsPT; ++q) {
+                    const uint32_t gw = g[b][q >> 1];
+                    y[q] = acc[q] * ((q & 1) ? bf16_hi(gw) : bf16_lo(gw));
+                }
+                st_u2(p.out + t * H + col, make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3])));
+            }
+        }
+    } else if constexpr (!FUSED) {
         // ---- plain finalize: every tile goes straight to out ----------------
         for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
             bool ok = true;
@@ -346,12 +450,18 @@ using StreamKernel = void (*)(const Params, const int, const int);
 
 template <int MAXTILES>
 StreamKernel pick(bool fused, bool fp4) {
-    if (fp4) return fused ? stream_kernel<MAXTILES, true, true> : nullptr;
-    return fused ? stream_kernel<MAXTILES, true, false> : stream_kernel<MAXTILES, false, false>;
+    if (fp4) return fused ? stream_kernel<MAXTILES, true, true, false> : nullptr;
+    return fused ? stream_kernel<MAXTILES, true, false, false> : stream_kernel<MAXTILES, false, false, false>;
 }
 
-StreamKernel stream_kernel_for(int H, bool fused, bool fp4) {
+StreamKernel stream_kernel_for(int H, bool fused, bool fp4, bool en) {
     const int tiles = (H + kStreamCB - 1) / kStreamCB;
+    if (en) {
+        if (fused || fp4) return nullptr;
+        if (tiles <= 2) return stream_kernel<2, false, false, true>;
+        if (tiles <= 4) return stream_kernel<4, false, false, true>;
+        return nullptr;
+    }
     if (tiles <= 2) return pick<2>(fused, fp4);
     if (tiles <= 4) return pick<4>(fused, fp4);
     if (tiles <= 8) return pick<8>(fused, fp4);
@@ -370,14 +480,14 @@ int stream_smem_bytes(int k, int nstages, bool fused) {
     return ((2 * nstages * 8 + 127) / 128) * 128 + nstages * stream_stage_bytes(k, fused);
 }
 
-cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes) {
-    StreamKernel kf = stream_kernel_for(H, fused, fp4);
+cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en) {
+    StreamKernel kf = stream_kernel_for(H, fused, fp4, en);
     if (!kf) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    StreamKernel kf = stream_kernel_for(p.H, l.fused != 0, l.fp4 != 0);
+    StreamKernel kf = stream_kernel_for(p.H, l.fused != 0, l.fp4 != 0, l.expert_norm != 0);
     if (!kf) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid_x), 1, 1);

@@ -334,3 +334,11 @@ def nvfp4_quantize(*a, **kw):
 
 def finalize_residual_rmsnorm_nvfp4(*a, **kw):
     return default().finalize_residual_rmsnorm_nvfp4(*a, **kw)
+
+
+def expert_rmsnorm_f64(*a, **kw):
+    return default().expert_rmsnorm_f64(*a, **kw)
+
+
+def finalize_expert_rmsnorm(*a, **kw):
+    return default().finalize_expert_rmsnorm(*a, **kw)

@@ -75,3 +75,19 @@ def oracle_finalize_only(inputs: dict, tokens=None):
     """The oracle's plain finalize on host copies: (out_bits, bad_slots)."""
     return oracle.finalize_only(bf16_bits(inputs["expert_out"]), inputs["permuted_row_of"].cpu().numpy(),
                                 f32(inputs["topk_weights"]), tokens=tokens)
+
+
+def oracle_expert_norm(inputs: dict, tokens=None):
+    """The oracle's per-expert RMSNorm finalize on host copies:
+    (out_bits, y float64, s float64, bad_slots), where y is the exact value
+    before rounding and s the same sum over |w|, |E| and |gamma| (the scale
+    of the FP32 rounding error of any evaluation order)."""
+    E = bf16_bits(inputs["expert_out"])
+    idx = inputs["permuted_row_of"].cpu().numpy()
+    w = f32(inputs["topk_weights"])
+    g = bf16_bits(inputs["gamma"])
+    out, bad = oracle.finalize_expert_rmsnorm(E, idx, w, g, inputs["eps"], tokens=tokens)
+    y, _ = oracle.expert_rmsnorm_f64(E, idx, w, g, inputs["eps"], tokens=tokens)
+    s, _ = oracle.expert_rmsnorm_f64(E & np.uint16(0x7FFF), idx, np.abs(w), g & np.uint16(0x7FFF),
+                                     inputs["eps"], tokens=tokens)
+    return out, y, s, bad
