@@ -71,11 +71,13 @@ int auto_cluster(int chunks) {
 }
 
 // Variant choice by the number of elements T*H of a call (measured on GB300
-// with cold inputs): up to 2^18 a cluster of 8 CTAs per token is fastest (few
-// tokens, latency bound); up to 3*2^20 one CTA per token; beyond that the
-// persistent ring kernel, whose per-SM pipeline needs enough tokens per SM.
+// with cold inputs, CUDA graph): up to 2^18 a cluster of 8 CTAs per token is
+// fastest (few tokens, latency bound); below 1.5*2^20 one CTA per token; from
+// there the persistent ring kernel (its per-SM pipeline needs a few tokens per
+// SM: at 1.5*2^20 it is 8 % faster at H = 4096 and 3 % slower at H = 8192, at
+// 2^21 faster at both, at 3*2^20 by 9-15 %).
 constexpr int64_t kClusterMaxElems = int64_t(1) << 18;
-constexpr int64_t kRowsMaxElems = int64_t(3) << 20;
+constexpr int64_t kRowsMaxElems = int64_t(3) << 19;
 constexpr int64_t kEarlyTriggerMaxElems = int64_t(1) << 19;
 constexpr int kMaxStages = 8;
 

@@ -88,7 +88,8 @@ def test_expert_norm_stress_values_and_repeats():
     assert np.array_equal(got, again)
 
 
-def test_expert_norm_bad_and_sentinel_slots():
+@pytest.mark.parametrize("variant", [mfr.VARIANT_ROWS, mfr.VARIANT_STREAM], ids=["rows", "ring"])
+def test_expert_norm_bad_and_sentinel_slots(variant):
     inp = W.make_inputs(W.decode(8), "cuda")
     idx = inp["permuted_row_of"].clone()
     idx[2, 5] = -1
@@ -96,13 +97,13 @@ def test_expert_norm_bad_and_sentinel_slots():
     inp["permuted_row_of"] = idx
     want, y, s, bad = oracle_expert_norm(inp)
     assert bad == 2
-    got, plan = run_expert_norm(inp)
+    got, plan = run_expert_norm(inp, variant=variant)
     assert_expert_norm_close(got, want, y, s)
     assert plan.get_status() & mfr.STATUS_BAD_INDEX
     # with sentinel_skip a negative index is a skipped non-local slot, not an error;
-    # the out-of-range positive one still is
+    # the out-of-range positive one was replaced by a valid row
     idx[6, 0] = idx[6, 1]
-    got, plan = run_expert_norm(inp, sentinel_skip=True)
+    got, plan = run_expert_norm(inp, sentinel_skip=True, variant=variant)
     want, y, s, _ = oracle_expert_norm(inp)
     assert_expert_norm_close(got, want, y, s)
     assert plan.get_status() == 0
