@@ -62,12 +62,28 @@ int pick_cpt(int chunks) {
     return 0;
 }
 
-// Cluster size for the split-H variant: the largest power of two <= 8 that
-// divides the chunk count and leaves at least one warp of chunks per CTA.
-int auto_cluster(int chunks) {
-    int c = 8;
+// Cluster size for the split-H variant: the largest power of two <= cmax
+// that divides the chunk count and leaves at least one warp of chunks per CTA.
+int auto_cluster(int chunks, int cmax = 8) {
+    int c = cmax;
     while (c > 1 && (chunks % c != 0 || chunks / c < 32)) c /= 2;
     return c;
+}
+
+// Cluster size for a latency-bound call of T*H = elems (measured on GB300, a
+// CUDA graph of back-to-back calls, cold inputs, H = 4096 and 8192): up to
+// 2^14 elements the fewest CTAs that give each 128 threads (one 16-byte chunk
+// per thread: H=4096 -> 4, H=8192 -> 8; 3 % faster than 8 at H=4096, T=1);
+// up to 2^17 clusters of 16 (4-9 % faster than 8 at T = 4..32, H = 4096 and
+// T = 4..16, H = 8192); beyond, 8 (16 is 7 % slower at T=32, H=8192).
+int decode_cluster(int chunks, int64_t elems) {
+    if (elems <= (int64_t(1) << 14)) {
+        int c = 1;
+        while (c < 16 && chunks / (2 * c) >= 128 && chunks % (2 * c) == 0) c *= 2;
+        return c;
+    }
+    if (elems <= (int64_t(1) << 17)) return auto_cluster(chunks, 16);
+    return auto_cluster(chunks);
 }
 
 // Variant choice by the number of elements T*H of a call (measured on GB300
@@ -193,7 +209,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     if (variant == MFR_VARIANT_AUTO) {
         const int64_t elems = T * H;
         if (elems <= kClusterMaxElems) {
-            if (csize == 0) csize = auto_cluster(chunks);
+            if (csize == 0) csize = decode_cluster(chunks, elems);
             variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
         } else if (elems < kRowsMaxElems || stages < 2) {
             variant = MFR_VARIANT_ROWS;
