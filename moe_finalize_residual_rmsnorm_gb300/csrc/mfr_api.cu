@@ -188,8 +188,8 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     int csize = o.cluster_size;
     // ring depth the bulk-copy kernel would get on this device
     const int stage_bytes = mfr::stream_stage_bytes(k, fused);
-    // room left for the kernels' static shared memory (at most ~1.2 KB: the
-    // per-expert RMSNorm mode's double-buffered slot sums) and slack
+    // room left for the ring kernel's static shared memory (640 bytes in its
+    // per-expert RMSNorm mode, the largest) and slack
     const int ring_budget = smem_optin - 2048;
     int stages = 0;
     while (stages < kMaxStages && mfr::stream_smem_bytes(k, stages + 1, fused) <= ring_budget) ++stages;
