@@ -163,17 +163,18 @@ __device__ __forceinline__ uint32_t e2m1x2_rn_sat(float lo, float hi) {
 // values each, lane 2m holding the first eight).  All 32 lanes must call it.
 //   amax = max |y|;  sf = E4M3((amax / 6) * s_enc);  dec = value(sf) / s_enc;
 //   enc = sf == 0 ? 0 : 1 / dec;  q_i = E2M1(y_i * enc)
-// Every step is one correctly rounded FP32 operation.  Returns this lane's
-// eight codes packed into 4 bytes (element 0 in the lowest nibble) and the
-// block's scale byte in *sf.
-__device__ __forceinline__ uint32_t nvfp4_block8(const float (&y)[8], float s_enc, uint32_t* sf) {
+// Every step is one correctly rounded FP32 operation; enc depends on sf
+// alone, so it is read from enc_tab[sf], the 256 values computed once per
+// call with the same two divisions.  Returns this lane's eight codes packed
+// into 4 bytes (element 0 in the lowest nibble) and the scale byte in *sf.
+__device__ __forceinline__ uint32_t nvfp4_block8(const float (&y)[8], float s_enc, const float* enc_tab,
+                                                 uint32_t* sf) {
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(y[i]));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
     const uint32_t s8 = e4m3_rn_sat(__fmul_rn(__fdiv_rn(amax, 6.0f), s_enc));
-    const float dec = __fdiv_rn(e4m3_to_f32(s8), s_enc);
-    const float enc = (s8 == 0u) ? 0.f : __fdiv_rn(1.0f, dec);
+    const float enc = enc_tab[s8];
     uint32_t w = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -183,16 +184,18 @@ __device__ __forceinline__ uint32_t nvfp4_block8(const float (&y)[8], float s_en
 }
 
 // The same for a 16-element block held by a lane quad (lanes 4m..4m+3, four
-// values each, in column order).  Returns this lane's four codes in 2 bytes.
-__device__ __forceinline__ uint32_t nvfp4_block4(const float (&y)[4], float s_enc, uint32_t* sf) {
+// values each, in column order), with enc read from enc_tab[s8] (the 256
+// values 1 / (value(s8) / s_enc) computed once per call, 0 at s8 = 0).
+// Returns this lane's four codes in 2 bytes.
+__device__ __forceinline__ uint32_t nvfp4_block4(const float (&y)[4], float s_enc, const float* enc_tab,
+                                                 uint32_t* sf) {
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(y[i]));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
     const uint32_t s8 = e4m3_rn_sat(__fmul_rn(__fdiv_rn(amax, 6.0f), s_enc));
-    const float dec = __fdiv_rn(e4m3_to_f32(s8), s_enc);
-    const float enc = (s8 == 0u) ? 0.f : __fdiv_rn(1.0f, dec);
+    const float enc = enc_tab[s8];
     const uint32_t w = e2m1x2_rn_sat(__fmul_rn(y[0], enc), __fmul_rn(y[1], enc)) |
                        (e2m1x2_rn_sat(__fmul_rn(y[2], enc), __fmul_rn(y[3], enc)) << 8);
     *sf = s8;

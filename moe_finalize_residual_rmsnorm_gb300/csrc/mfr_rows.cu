@@ -64,6 +64,7 @@ rows_kernel(const Params p, const int csize)
     __shared__ float s_w[kMaxK];
     __shared__ float s_warp[kRowsMaxThreads / 32];
     __shared__ float s_part[16 * (kRowsMaxThreads / 32)];   // cluster: (rank, warp) partials
+    __shared__ float s_enc_tab[FP4 ? 256 : 1];               // FP4: encode scale per scale byte
 
     if (p.early_trigger)
         pdl_launch_dependents();   // the next kernel may start its prologue now
@@ -98,6 +99,12 @@ rows_kernel(const Params p, const int csize)
         const int c = tid + i * nthreads;
         g[i] = (FUSED && c < nck) ? *reinterpret_cast<const uint4*>(p.gamma + col0 + c * 8)
                                   : make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (FP4) {
+        // enc(s8) = 1 / (value(s8) / s_enc), 0 for s8 = 0: the two divisions
+        // of each block done once per scale byte, before the wait
+        for (int i = tid; i < 256; i += nthreads)
+            s_enc_tab[i] = i == 0 ? 0.f : __fdiv_rn(1.0f, __fdiv_rn(e4m3_to_f32(static_cast<uint32_t>(i)), p.s_enc));
     }
     __syncthreads();
 
@@ -271,7 +278,7 @@ rows_kernel(const Params p, const int csize)
 #pragma unroll
             for (int q = 0; q < 8; ++q) y[q] = (c < nck) ? acc[i][q] * inv * gf[q] : 0.f;
             uint32_t sf;
-            const uint32_t w = nvfp4_block8(y, p.s_enc, &sf);
+            const uint32_t w = nvfp4_block8(y, p.s_enc, s_enc_tab, &sf);
             if (c < nck) {
                 const int64_t col = col0 + static_cast<int64_t>(c) * 8;
                 *reinterpret_cast<uint32_t*>(p.out_q + t * (p.H / 2) + col / 2) = w;

@@ -75,6 +75,11 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     __shared__ float s_warp[kStreamNT / 32];
     __shared__ float s_slot[EN ? kStreamNT / 32 : 1][EN ? 8 : 1];   // EN: per-warp slot sums
     __shared__ float s_coef[EN ? 8 : 1];                            // EN: c_j of the token
+    // FP4: the encode scale of every E4M3 block-scale byte for this call's
+    // s_enc, enc(s8) = 1 / (value(s8) / s_enc), 0 for s8 = 0, each step the
+    // same correctly rounded FP32 operation as per block: two divisions per
+    // block become one table read
+    __shared__ float s_enc_tab[FP4 ? 256 : 1];
     __shared__ int s_abort;
 
     const int tid = threadIdx.x;
@@ -91,6 +96,10 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
         }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if constexpr (FP4) {
+        for (int i = tid; i < 256; i += blockDim.x)
+            s_enc_tab[i] = i == 0 ? 0.f : __fdiv_rn(1.0f, __fdiv_rn(e4m3_to_f32(static_cast<uint32_t>(i)), p.s_enc));
     }
     __syncthreads();
 
@@ -466,7 +475,7 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
 #pragma unroll
                 for (int q = 0; q < kColsPT; ++q) if (col >= H) y[q] = 0.f;
                 uint32_t sf;
-                const uint32_t w = nvfp4_block4(y, p.s_enc, &sf);
+                const uint32_t w = nvfp4_block4(y, p.s_enc, s_enc_tab, &sf);
                 if (col < H) {
                     *reinterpret_cast<uint16_t*>(p.out_q + t * (H / 2) + col / 2) = static_cast<uint16_t>(w);
                     if ((tid & 3) == 0) p.out_sf[t * (H / 16) + col / 16] = static_cast<uint8_t>(sf);
