@@ -75,24 +75,29 @@ int auto_cluster(int chunks, int cmax = 8) {
 // 2^14 elements the fewest CTAs that give each 128 threads (one 16-byte chunk
 // per thread: H=4096 -> 4, H=8192 -> 8; 3 % faster than 8 at H=4096, T=1);
 // up to 2^17 clusters of 16 (4-9 % faster than 8 at T = 4..32, H = 4096 and
-// T = 4..16, H = 8192); beyond, 8 (16 is 7 % slower at T=32, H=8192).
+// T = 4..16, H = 8192); up to 2^18, 8 (16 is 7 % slower at T=32, H=8192); up
+// to 2^19 the fewest CTAs of 256 threads each (H=4096 -> 2, H=8192 -> 4: 3-5 %
+// faster than one CTA per token at H=4096, 9-18 % at H=8192).  1 = no cluster.
 int decode_cluster(int chunks, int64_t elems) {
-    if (elems <= (int64_t(1) << 14)) {
+    auto split = [chunks](int threads) {
         int c = 1;
-        while (c < 16 && chunks / (2 * c) >= 128 && chunks % (2 * c) == 0) c *= 2;
+        while (c < 16 && chunks / (2 * c) >= threads && chunks % (2 * c) == 0) c *= 2;
         return c;
-    }
+    };
+    if (elems <= (int64_t(1) << 14)) return split(128);
     if (elems <= (int64_t(1) << 17)) return auto_cluster(chunks, 16);
-    return auto_cluster(chunks);
+    if (elems <= (int64_t(1) << 18)) return auto_cluster(chunks);
+    return split(256);
 }
 
 // Variant choice by the number of elements T*H of a call (measured on GB300
-// with cold inputs, CUDA graph): up to 2^18 a cluster of 8 CTAs per token is
-// fastest (few tokens, latency bound); below 1.5*2^20 one CTA per token; from
+// with cold inputs, CUDA graph): up to 2^19 a cluster of CTAs per token is
+// fastest (few tokens, latency bound; decode_cluster picks its size); below
+// 1.5*2^20 one CTA per token; from
 // there the persistent ring kernel (its per-SM pipeline needs a few tokens per
 // SM: at 1.5*2^20 it is 8 % faster at H = 4096 and 3 % slower at H = 8192, at
 // 2^21 faster at both, at 3*2^20 by 9-15 %).
-constexpr int64_t kClusterMaxElems = int64_t(1) << 18;
+constexpr int64_t kClusterMaxElems = int64_t(1) << 19;
 constexpr int64_t kRowsMaxElems = int64_t(3) << 19;
 constexpr int64_t kEarlyTriggerMaxElems = int64_t(1) << 19;
 constexpr int kMaxStages = 8;
