@@ -69,7 +69,9 @@ int setup_device(int dev, DeviceSetup* out) {
             cudaGetLastError();
             return MFR_ERR_CUDA;
         }
-        const int budget = optin - 1024;
+        // the same budget as the planned path (mfr_api.cu), so whichever sets
+        // the per-kernel attribute last, every ring either path picks fits it
+        const int budget = optin - 2048;
         // one attribute per kernel instantiation (by column tiles per token),
         // set to the device maximum exactly as the planned path sets it
         for (int h : {4096, 8192, 16384}) {

@@ -111,3 +111,20 @@ def test_noalloc_allocates_nothing_through_torch(lib):
     want_res, want_out = _planned(inp)
     assert np.array_equal(f32(rout).view(np.uint32), want_res.view(np.uint32))
     assert_out_close(bf16_bits(out), want_out)
+
+
+def test_noalloc_ring_fits_after_a_plan_set_the_kernel_attribute(lib):
+    """Plans and the allocation-free call set the same per-kernel shared-memory
+    attribute; with k=5 the deepest ring the budget allows is 8 stages, which
+    must still launch after a plan has set the attribute."""
+    wl = W.PREFILL.with_(T=400, k=5)
+    inp = W.make_inputs(wl, "cuda")
+    want_res, want_out = _planned(inp)       # makes a plan: sets the attribute
+    rout = torch.empty_like(inp["residual"])
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    st = ctypes.c_int(-1)
+    assert _call_noalloc(lib, inp, rout, out, slot=7, status=st) == 0, lib.moe_finalize_rmsnorm_last_error()
+    assert st.value == 0
+    torch.cuda.synchronize()
+    assert_residual_close(f32(rout), want_res)
+    assert_out_close(bf16_bits(out), want_out)
