@@ -97,8 +97,8 @@ typedef struct mfr_options {
 /* What a plan decided; for tests, benchmarks and logs. */
 typedef struct mfr_plan_info {
     int variant;       /* MFR_VARIANT_CLUSTER / _ROWS / _STREAM */
-    int grid_x;        /* CTAs launched along x (cluster rank, or persistent CTA id) */
-    int grid_y;        /* CTAs along y (tokens for CLUSTER) */
+    int grid_x;        /* CTAs launched (tokens x cluster size, or persistent CTAs) */
+    int grid_y;        /* always 1 */
     int block;         /* threads per CTA */
     int cluster;       /* CTAs per cluster (1 = none) */
     int smem_bytes;    /* dynamic shared memory per CTA */
@@ -242,8 +242,10 @@ void moe_finalize_rmsnorm_destroy(mfr_plan_t plan);
  *     inv_j     = rsqrt(mean_h(E[r_j, :]^2) + eps)          (FP32, per row)
  *     out[t, h] = bf16( sum_j w[t,j] * ((E[r_j, h] * inv_j) * gamma[h]) )
  * with r_j = permuted_row_of[t, j], FP32 fused multiply-adds in slot order
- * j = 0..k-1, the shared gamma, and no residual.  One CTA per token
- * (MFR_VARIANT_ROWS; AUTO picks it, CLUSTER and STREAM are refused).
+ * j = 0..k-1, the shared gamma, and no residual.  Two kernels: one CTA per
+ * token (MFR_VARIANT_ROWS), and for T*H >= 1.5*2^20 with k <= 8 and
+ * H <= 8192 the persistent ring kernel (MFR_VARIANT_STREAM; forcing it
+ * outside those limits is MFR_ERR_UNSUPPORTED_SHAPE); CLUSTER is refused.
  *
  * moe_finalize_expert_rmsnorm_plan: as moe_finalize_rmsnorm_plan (same
  * shape rules and options; cluster_size is ignored).
