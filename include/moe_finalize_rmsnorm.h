@@ -33,8 +33,8 @@
  * Conventions for every entry point:
  *  - Pointers named "device" are CUDA device (or managed) addresses on the
  *    plan's device; the caller owns all of them.  No entry point allocates on
- *    a run: only moe_finalize_rmsnorm_plan allocates (a 4-byte device status
- *    word), and moe_finalize_rmsnorm_destroy frees it.
+ *    a run: only the *_plan functions allocate (a 4-byte device status word
+ *    each), and moe_finalize_rmsnorm_destroy frees it.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Runs are asynchronous on that stream.
  *  - Every function returns MFR_OK or an MFR_ERR_* code and never aborts the
