@@ -104,10 +104,8 @@ expert_norm_kernel(const Params p)
 #pragma unroll
             for (int i = 0; i < CPT; ++i) {
                 if (tid + i * nthreads < nck) {
-                    float e[8];
-                    unpack8(v[s][i], e);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) ss = __fmaf_rn(e[q], e[q], ss);
+                    ss = sumsq_bf16x4(make_uint2(v[s][i].x, v[s][i].y), ss);
+                    ss = sumsq_bf16x4(make_uint2(v[s][i].z, v[s][i].w), ss);
                 }
             }
             ss = warp_allreduce_sum(ss);

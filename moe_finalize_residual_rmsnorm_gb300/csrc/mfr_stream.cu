@@ -258,9 +258,7 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                     if (j < k && (mask & (1u << j)) && mine) {
                         const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
                         rv[b][j] = v;
-                        const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
-#pragma unroll
-                        for (int q = 0; q < kColsPT; ++q) ss[j] = __fmaf_rn(e[q], e[q], ss[j]);
+                        ss[j] = sumsq_bf16x4(v, ss[j]);   // bf16 operands straight into the FMA
                     }
                 }
                 __syncwarp();
