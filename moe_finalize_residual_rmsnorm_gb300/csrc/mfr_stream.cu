@@ -1,6 +1,7 @@
 // Persistent bulk-copy kernel (MFR_VARIANT_STREAM).
 //
-// One CTA per SM walks a static list of tokens (t = blockIdx.x, += gridDim.x).
+// At most one CTA per SM walks a static list of tokens (t = blockIdx.x,
+// += gridDim.x); the grid spreads the tokens evenly (stream_grid in mfr_api.cu).
 // A producer warp stages, for each token and each column tile of width
 // CB = 2048, the k gathered expert-row segments and the residual segment
 // into a ring of shared-memory stages with bulk asynchronous copies
@@ -19,9 +20,11 @@
 // with an RMSNorm per expert row, the reading of the PR 6544 analysis, section
 // 2.1 (see mfr_expert_norm.cu): each consumer thread keeps its four columns
 // of every slot and tile packed in registers while it sums each slot's
-// squares, the CTA reduces the k sums (warp butterfly, then warps in index
-// order), c_j = w_j * rsqrt(ss_j / H + eps), and out = bf16(gamma *
-// sum_j c_j * e_j) with FMAs in slot order.  The stages carry only the rows.
+// squares (bf16 operands straight into the FMA), the CTA reduces the k sums
+// (a reduce-scatter butterfly in each warp, then thread j adds slot j over
+// the warps in index order), c_j = w_j * rsqrt(ss_j / H + eps), and
+// out = bf16(gamma * sum_j c_j * e_j) with FMAs in slot order.  The stages
+// carry only the rows.
 //
 // The ring keeps several tiles in flight per SM at all times, so the gather
 // never drains between tokens (the register-gather kernel stalls on each
