@@ -8,8 +8,10 @@
 //               entry when the grid is small (few tokens: its CTAs leave room),
 //               else after the loads, so a following kernel does not park CTAs
 //               on every SM for the whole call
-//   prologue  : slot indices and weights of t, gamma; ask L2 to prefetch the
-//               CTA's row and residual segments             (before the PDL wait)
+//   prologue  : slot indices and weights of t (into registers with RS), gamma,
+//               (FP4) the encode scale of each of the 256 scale bytes; ask L2
+//               to prefetch the CTA's row and residual segments; complete the
+//               cluster barrier                             (before the PDL wait)
 //   wait      : the producer of expert_out / residual_in has finished
 //   gather    : k rows of expert_out, 16 bytes per load, all loads of a slot
 //               group issued before any is used
