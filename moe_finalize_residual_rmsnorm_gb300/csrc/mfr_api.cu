@@ -200,9 +200,11 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     while (stages < kMaxStages && mfr::stream_smem_bytes(k, stages + 1, fused) <= ring_budget) ++stages;
     if (expert_norm) {
         // one CTA per token (mfr_expert_norm.cu), or the ring kernel, which
-        // keeps each thread's share of the token's rows in registers: k <= 8
-        // and at most 4 column tiles (H <= 8192)
-        const bool ring_ok = k <= 8 && H <= 8192 && stages >= 2;
+        // keeps a token's rows available until its slot scales are known: k <= 8,
+        // at most 4 column tiles (H <= 8192), and a ring that holds a whole
+        // token when it has more than 2 tiles
+        const int tiles = mfr::stream_tiles(static_cast<int>(H));
+        const bool ring_ok = k <= 8 && H <= 8192 && stages >= 2 && (tiles <= 2 || stages >= tiles);
         if (variant == MFR_VARIANT_CLUSTER)
             return fail(MFR_ERR_INVALID_ARG, "the per-expert RMSNorm finalize has no cluster variant");
         if (variant == MFR_VARIANT_STREAM && !ring_ok)

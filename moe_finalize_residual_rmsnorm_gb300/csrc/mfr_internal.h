@@ -70,6 +70,7 @@ cudaError_t expert_norm_launch(const Params& p, const Launch& l, cudaStream_t s)
 
 // mfr_stream.cu: persistent CTAs fed by bulk copies into a shared-memory ring.
 int stream_threads();
+int stream_tiles(int H);   // column tiles of a token
 // Persistent CTAs for T tokens on `sms` SMs: the fewest rounds of one token per
 // CTA, over as few CTAs as give every CTA the same number of tokens (+-1).
 int stream_grid(int64_t T, int sms);

@@ -218,8 +218,7 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     for (int b = 0; b < MAXTILES; ++b) {
         const int col = b * kStreamCB + tid * kColsPT;
         uint2 v = make_uint2(0, 0);
-        if ((FUSED || (EN && MAXTILES <= 2)) && b < ntiles && col < H)
-            v = *reinterpret_cast<const uint2*>(p.gamma + col);
+        if ((FUSED || EN) && b < ntiles && col < H) v = *reinterpret_cast<const uint2*>(p.gamma + col);
         g[b][0] = v.x; g[b][1] = v.y;
     }
     pdl_wait();
@@ -227,16 +226,26 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     int s = 0;
     uint32_t phase = 0;
     if constexpr (EN) {
-        // ---- RMSNorm per expert row: rows kept packed until the token's c_j are known
+        // ---- RMSNorm per expert row: the rows stay available until the token's c_j are known.
+        // With at most 2 tiles a thread keeps its share of them packed in
+        // registers and releases each stage at once; with more (H > 4096) the
+        // stages themselves are held until the second pass re-reads them, so
+        // no registers hold rows (a token's tiles fit in the ring: the plan
+        // checks stages >= tiles) and the producer refills only the stages
+        // left over.  Measured at H = 8192: holding stages is faster than 64
+        // registers of packed rows.
+        constexpr bool kHold = MAXTILES > 2;
         const int lane = tid & 31;
         for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
-            uint2 rv[MAXTILES][8];
+            uint2 rv[kHold ? 1 : MAXTILES][kHold ? 1 : 8];
             float ss[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) ss[j] = 0.f;
             uint32_t mask = 0;
             float my_w = 0.f;       // thread j < 8: the weight of slot j
             bool ok = true;
+            const int s0 = s;
+            const uint32_t phase0 = phase;
 #pragma unroll
             for (int b = 0; b < MAXTILES; ++b) {
                 if (b >= ntiles) break;
@@ -257,15 +266,17 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 const bool mine = tid * kColsPT < min(kStreamCB, H - c0);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    rv[b][j] = make_uint2(0, 0);
+                    if constexpr (!kHold) rv[b][j] = make_uint2(0, 0);
                     if (j < k && (mask & (1u << j)) && mine) {
                         const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
-                        rv[b][j] = v;
+                        if constexpr (!kHold) rv[b][j] = v;
                         ss[j] = sumsq_bf16x4(v, ss[j]);   // bf16 operands straight into the FMA
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ebar);     // this warp is done with the stage
+                if constexpr (!kHold) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ebar);     // this warp is done with the stage
+                }
             }
             // Per-slot sums over the CTA in a fixed order.  In the warp, a
             // reduce-scatter butterfly (xor 16, 8, 4 halve the slots a lane
@@ -308,46 +319,49 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 s_coef[tid] = my_w * rsqrtf(tot / static_cast<float>(H) + p.eps);
             }
             asm volatile("bar.sync 1, %0;" :: "r"(kStreamNT) : "memory");   // s_coef ready, s_slot reusable
-            // Up to 2 tiles gamma and c_j stay in registers; with 4 tiles the 64
-            // registers of packed rows leave no room (17 warps: at most 96 per
-            // thread), so gamma comes from L1 (the same for every token) and
-            // c_j from shared memory at each use (measured: no spill, 156 ->
-            // 143 us at H = 8192; at H = 4096 the register form is 30 % faster).
-            constexpr bool kLean = MAXTILES > 2;
             float cr[8];
-            if constexpr (!kLean) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) cr[j] = (j < k) ? s_coef[j] : 0.f;
-            }
+            for (int j = 0; j < 8; ++j) cr[j] = (j < k) ? s_coef[j] : 0.f;
+            int s2 = s0;
+            uint32_t phase2 = phase0;
 #pragma unroll
             for (int b = 0; b < MAXTILES; ++b) {
                 if (b >= ntiles) break;
                 const int col = b * kStreamCB + tid * kColsPT;
-                if (col >= H) continue;
-                uint2 gv;
-                if constexpr (kLean) gv = *reinterpret_cast<const uint2*>(p.gamma + col);
-                else gv = make_uint2(g[b][0], g[b][1]);
+                const unsigned char* st = stages + static_cast<size_t>(s2) * stage_bytes;
+                const uint32_t ebar = smem_u32(&bars[nstages + s2]);
+                if (++s2 == nstages) { s2 = 0; phase2 ^= 1u; }
                 float acc[kColsPT];
 #pragma unroll
                 for (int q = 0; q < kColsPT; ++q) acc[q] = 0.f;
+                if (col < H) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (j < k && (mask & (1u << j))) {
-                        const float cj = kLean ? s_coef[j] : cr[j];
-                        const uint2 v = rv[b][j];
-                        const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+                    for (int j = 0; j < 8; ++j) {
+                        if (j < k && (mask & (1u << j))) {
+                            uint2 v;
+                            if constexpr (kHold) v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
+                            else v = rv[b][j];
+                            const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
 #pragma unroll
-                        for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(cj, e[q], acc[q]);
+                            for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(cr[j], e[q], acc[q]);
+                        }
                     }
                 }
-                float y[kColsPT];
-#pragma unroll
-                for (int q = 0; q < kColsPT; ++q) {
-                    const uint32_t gw = (q >> 1) ? gv.y : gv.x;
-                    y[q] = acc[q] * ((q & 1) ? bf16_hi(gw) : bf16_lo(gw));
+                if constexpr (kHold) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ebar);     // both passes are done with the stage
                 }
-                st_u2(p.out + t * H + col, make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3])));
+                if (col < H) {
+                    float y[kColsPT];
+#pragma unroll
+                    for (int q = 0; q < kColsPT; ++q) {
+                        const uint32_t gw = g[b][q >> 1];
+                        y[q] = acc[q] * ((q & 1) ? bf16_hi(gw) : bf16_lo(gw));
+                    }
+                    st_u2(p.out + t * H + col, make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3])));
+                }
             }
+            (void)phase2;
         }
     } else if constexpr (!FUSED) {
         // ---- plain finalize: every tile goes straight to out ----------------
@@ -514,6 +528,8 @@ StreamKernel stream_kernel_for(int H, bool fused, bool fp4, bool en) {
 }  // namespace
 
 int stream_threads() { return kStreamThreads; }
+
+int stream_tiles(int H) { return (H + kStreamCB - 1) / kStreamCB; }
 
 int stream_stage_bytes(int k, bool fused) {
     return kHeaderBytes + k * kStreamCB * 2 + (fused ? kStreamCB * 4 : 0);
