@@ -593,8 +593,10 @@ def run_reference(args):
     inp = W.make_inputs(wl, "cpu")
     host = host_copy(inp)
     cores = host_cores()
+    # the whole run (warm-up + timed steps) stays within ~150 s of oracle work
+    # for any --steps / --warmup: each step gets an equal share, at least 20 ms
     total_budget = 150.0
-    per_step = max(0.5, min(args.cpu_seconds, total_budget / max(1, args.steps + args.warmup)))
+    per_step = max(0.02, min(args.cpu_seconds, total_budget / max(1, args.steps + args.warmup)))
     n_tokens = calibrate_tokens(host, wl.T, per_step, cores)
     for i in range(args.warmup):
         time_oracle(host, n_tokens, cores, 100 + i)
