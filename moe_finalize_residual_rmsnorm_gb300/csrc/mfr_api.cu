@@ -53,54 +53,6 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-int round_up(int v, int m) { return (v + m - 1) / m * m; }
-
-// Smallest chunks-per-thread that keeps a CTA within kRowsMaxThreads threads.
-int pick_cpt(int chunks) {
-    for (int cpt : {1, 2, 4})
-        if ((chunks + cpt - 1) / cpt <= mfr::kRowsMaxThreads) return cpt;
-    return 0;
-}
-
-// Cluster size for the split-H variant: the largest power of two <= cmax
-// that divides the chunk count and leaves at least one warp of chunks per CTA.
-int auto_cluster(int chunks, int cmax = 8) {
-    int c = cmax;
-    while (c > 1 && (chunks % c != 0 || chunks / c < 32)) c /= 2;
-    return c;
-}
-
-// Cluster size for a latency-bound call of T*H = elems (measured on GB300, a
-// CUDA graph of back-to-back calls, cold inputs, H = 4096 and 8192): up to
-// 2^14 elements the fewest CTAs that give each 128 threads (one 16-byte chunk
-// per thread: H=4096 -> 4, H=8192 -> 8; 3 % faster than 8 at H=4096, T=1);
-// up to 2^17 clusters of 16 (4-9 % faster than 8 at T = 4..32, H = 4096 and
-// T = 4..16, H = 8192); up to 2^18, 8 (16 is 7 % slower at T=32, H=8192); up
-// to 2^19 the fewest CTAs of 256 threads each (H=4096 -> 2, H=8192 -> 4: 3-5 %
-// faster than one CTA per token at H=4096, 9-18 % at H=8192).  1 = no cluster.
-int decode_cluster(int chunks, int64_t elems) {
-    auto split = [chunks](int threads) {
-        int c = 1;
-        while (c < 16 && chunks / (2 * c) >= threads && chunks % (2 * c) == 0) c *= 2;
-        return c;
-    };
-    if (elems <= (int64_t(1) << 14)) return split(128);
-    if (elems <= (int64_t(1) << 17)) return auto_cluster(chunks, 16);
-    if (elems <= (int64_t(1) << 18)) return auto_cluster(chunks);
-    return split(256);
-}
-
-// Variant choice by the number of elements T*H of a call (measured on GB300
-// with cold inputs, CUDA graph): up to 2^19 a cluster of CTAs per token is
-// fastest (few tokens, latency bound; decode_cluster picks its size); below
-// 1.5*2^20 one CTA per token; from
-// there the persistent ring kernel (its per-SM pipeline needs a few tokens per
-// SM: at 1.5*2^20 it is 8 % faster at H = 4096 and 3 % slower at H = 8192, at
-// 2^21 faster at both, at 3*2^20 by 9-15 %).
-constexpr int64_t kClusterMaxElems = int64_t(1) << 19;
-constexpr int64_t kRowsMaxElems = int64_t(3) << 19;
-constexpr int64_t kEarlyTriggerMaxElems = int64_t(1) << 19;
-constexpr int kMaxStages = 8;
 
 }  // namespace
 
@@ -128,16 +80,6 @@ void moe_finalize_rmsnorm_default_options(mfr_options* opt) {
 
 }  // extern "C"
 
-namespace mfr {
-// T = 512 on 152 SMs: 128 CTAs x 4 tokens instead of 56 CTAs with 4 and 96
-// with 3 (measured 4 % faster at H = 8192, and never slower from T = 200 to
-// T = 16384: the last round no longer runs on a fraction of the SMs).
-int stream_grid(int64_t T, int sms) {
-    if (T <= sms) return static_cast<int>(T > 0 ? T : 1);
-    const int64_t rounds = (T + sms - 1) / sms;
-    return static_cast<int>((T + rounds - 1) / rounds);
-}
-}  // namespace mfr
 
 namespace {
 
@@ -181,73 +123,35 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         return fail(MFR_ERR_BAD_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a only",
                     dev, major, minor);
 
-    const int chunks = static_cast<int>(H / 8);
+    // ring depth the bulk-copy kernel would get on this device: room is left
+    // for the ring kernel's static shared memory (640 bytes in its per-expert
+    // RMSNorm mode, the largest) and slack
+    const int ring_budget = smem_optin - 2048;
+    int stages = 0;
+    while (stages < mfr::kMaxStages && mfr::stream_smem_bytes(k, stages + 1, fused) <= ring_budget) ++stages;
+
+    mfr::PolicyIn in{T, H, k, fused, fp4, expert_norm, o.force_variant, o.cluster_size, stages, sms};
+    mfr::PolicyOut pol{};
+    char why[200] = "";
+    const int prc = mfr::choose_launch(in, &pol, why, sizeof why, mfr::stream_threads());
+    if (prc != MFR_OK) return fail(prc, "%s", why);
+
     mfr::Launch l{};
     l.pdl = o.enable_pdl ? 1 : 0;
     l.grid_y = 1;
     l.fused = fused ? 1 : 0;
     l.fp4 = fp4 ? 1 : 0;
-    if (fp4 && H % 16 != 0)
-        return fail(MFR_ERR_UNSUPPORTED_SHAPE, "NVFP4 output needs H %% 16 == 0 (H=%lld)", (long long)H);
-    int variant = o.force_variant;
-    int csize = o.cluster_size;
-    // ring depth the bulk-copy kernel would get on this device
-    const int stage_bytes = mfr::stream_stage_bytes(k, fused);
-    // room left for the ring kernel's static shared memory (640 bytes in its
-    // per-expert RMSNorm mode, the largest) and slack
-    const int ring_budget = smem_optin - 2048;
-    int stages = 0;
-    while (stages < kMaxStages && mfr::stream_smem_bytes(k, stages + 1, fused) <= ring_budget) ++stages;
-    if (expert_norm) {
-        // one CTA per token (mfr_expert_norm.cu), or the ring kernel, which
-        // keeps a token's rows available until its slot scales are known: k <= 8,
-        // at most 4 column tiles (H <= 8192), and a ring that holds a whole
-        // token when it has more than 2 tiles
-        const int tiles = mfr::stream_tiles(static_cast<int>(H));
-        const bool ring_ok = k <= 8 && H <= 8192 && stages >= 2 && (tiles <= 2 || stages >= tiles);
-        if (variant == MFR_VARIANT_CLUSTER)
-            return fail(MFR_ERR_INVALID_ARG, "the per-expert RMSNorm finalize has no cluster variant");
-        if (variant == MFR_VARIANT_STREAM && !ring_ok)
-            return fail(MFR_ERR_UNSUPPORTED_SHAPE, "the per-expert RMSNorm ring kernel needs k <= 8 and H <= 8192");
-        if (variant == MFR_VARIANT_AUTO)
-            variant = (ring_ok && T * H >= kRowsMaxElems) ? MFR_VARIANT_STREAM : MFR_VARIANT_ROWS;
-        csize = 1;
-    }
-    if (variant == MFR_VARIANT_AUTO) {
-        const int64_t elems = T * H;
-        if (elems <= kClusterMaxElems) {
-            if (csize == 0) csize = decode_cluster(chunks, elems);
-            variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
-        } else if (elems < kRowsMaxElems || stages < 2) {
-            variant = MFR_VARIANT_ROWS;
-        } else {
-            variant = MFR_VARIANT_STREAM;
-        }
-    } else if (variant == MFR_VARIANT_CLUSTER) {
-        if (csize == 0) csize = auto_cluster(chunks);
-        if (csize < 2) csize = 2;
-    }
-    if (variant != MFR_VARIANT_CLUSTER) csize = 1;
-    // NVFP4 blocks of 16 columns must not straddle two CTAs of a cluster
-    while (fp4 && csize > 1 && (chunks / csize) % 2 != 0) csize /= 2;
-    if (variant == MFR_VARIANT_CLUSTER && csize < 2) variant = MFR_VARIANT_ROWS;
-    l.variant = variant;
     l.expert_norm = expert_norm ? 1 : 0;
-    // Signal dependents at kernel entry only while this grid is small: a
-    // large grid would let the next kernel park CTAs on every SM for the
-    // whole call (the ring kernel never signals early, see mfr_stream.cu).
-    l.early_trigger = (variant != MFR_VARIANT_STREAM && T * H <= kEarlyTriggerMaxElems) ? 1 : 0;
+    l.variant = pol.variant;
+    l.early_trigger = pol.early_trigger;
+    l.cluster = pol.cluster;
+    l.cpt = pol.cpt;
+    l.block = pol.block;
+    l.grid_x = pol.grid_x;
 
-    if (variant == MFR_VARIANT_STREAM) {
-        if (stages < 2)
-            return fail(MFR_ERR_UNSUPPORTED_SHAPE, "k=%d leaves room for fewer than 2 stages of %d bytes",
-                        k, stage_bytes);
-        l.cluster = 1;
-        l.cpt = 1;
-        l.block = mfr::stream_threads();
+    if (l.variant == MFR_VARIANT_STREAM) {
         l.stages = stages;
         l.smem_bytes = mfr::stream_smem_bytes(k, stages, fused);
-        l.grid_x = mfr::stream_grid(T, sms);
         // the attribute is per kernel, shared by every plan: always the device
         // maximum, so a plan with a deeper ring never loses its setting
         if ((e = mfr::stream_prepare(static_cast<int>(H), fused, fp4, ring_budget, expert_norm)) != cudaSuccess) {
@@ -255,15 +159,6 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }
     } else {
-        if (chunks % csize != 0)
-            return fail(MFR_ERR_UNSUPPORTED_SHAPE, "cluster of %d CTAs needs H/8 divisible by it (H=%lld)",
-                        csize, (long long)H);
-        const int cta_chunks = chunks / csize;
-        l.cluster = csize;
-        l.cpt = pick_cpt(cta_chunks);
-        if (l.cpt == 0) return fail(MFR_ERR_UNSUPPORTED_SHAPE, "H=%lld too wide", (long long)H);
-        l.block = round_up((cta_chunks + l.cpt - 1) / l.cpt, 32);
-        l.grid_x = static_cast<int>(T > 0 ? T * csize : csize);
         l.smem_bytes = 0;
         // Slot rows and weights in registers shorten the path from the
         // dependency wait to the data, unless the extra registers make the
@@ -287,13 +182,13 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }
-        if (csize > 1 && fused) {
+        if (l.cluster > 1 && fused) {
             int nclusters = 0;
             e = mfr::rows_max_active_clusters(l, &nclusters);
             if (e != cudaSuccess || nclusters < 1) {
                 cudaGetLastError();
                 return fail(MFR_ERR_UNSUPPORTED_SHAPE, "a cluster of %d CTAs x %d threads cannot be resident",
-                            csize, l.block);
+                            l.cluster, l.block);
             }
         }
     }

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "mfr_policy.h"
+
 namespace mfr {
 
 // Everything a kernel needs for one call; passed by value.
@@ -47,10 +49,6 @@ struct Launch {
     int expert_norm;  // 1: RMSNorm per expert row before the weighted sum (mfr_expert_norm.cu)
 };
 
-constexpr int kMaxK = 16;         // slots per token
-constexpr int kMaxH = 16384;      // hidden size
-constexpr int kRowsMaxThreads = 512;
-
 // Sets the calling thread's moe_finalize_rmsnorm_last_error() text.
 void set_last_error(const char* fmt, ...);
 
@@ -70,10 +68,6 @@ cudaError_t expert_norm_launch(const Params& p, const Launch& l, cudaStream_t s)
 
 // mfr_stream.cu: persistent CTAs fed by bulk copies into a shared-memory ring.
 int stream_threads();
-int stream_tiles(int H);   // column tiles of a token
-// Persistent CTAs for T tokens on `sms` SMs: the fewest rounds of one token per
-// CTA, over as few CTAs as give every CTA the same number of tokens (+-1).
-int stream_grid(int64_t T, int sms);
 int stream_stage_bytes(int k, bool fused);
 int stream_smem_bytes(int k, int nstages, bool fused);
 cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en = false);

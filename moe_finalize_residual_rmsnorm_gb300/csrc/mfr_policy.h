@@ -1,0 +1,185 @@
+// Launch policy of a plan: which kernel, how many CTAs per token, threads and
+// grid, from (T, H, k, the plan kind, the options, the ring depth the device
+// allows and its SM count).  Pure host code with no CUDA dependency, so the
+// CPU tests compile and check it directly; mfr_api.cu applies it.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cstdio>
+
+#include "moe_finalize_rmsnorm.h"
+
+namespace mfr {
+
+constexpr int kMaxK = 16;               // slots per token
+constexpr int kMaxH = 16384;            // hidden size
+constexpr int kRowsMaxThreads = 512;    // one-CTA-per-token kernels
+constexpr int kStreamTileCols = 2048;   // ring kernel: columns per tile
+constexpr int kMaxStages = 8;           // ring kernel: deepest ring
+
+// Variant choice by the number of elements T*H of a call (measured on GB300
+// with cold inputs, CUDA graph): up to 2^19 a cluster of CTAs per token is
+// fastest (few tokens, latency bound; decode_cluster picks its size); below
+// 1.5*2^20 one CTA per token; from there the persistent ring kernel (its
+// per-SM pipeline needs a few tokens per SM: at 1.5*2^20 it is 8 % faster at
+// H = 4096 and 3 % slower at H = 8192, at 2^21 faster at both, at 3*2^20 by
+// 9-15 %).  Small grids signal their dependents at entry.
+constexpr int64_t kClusterMaxElems = int64_t(1) << 19;
+constexpr int64_t kRowsMaxElems = int64_t(3) << 19;
+constexpr int64_t kEarlyTriggerMaxElems = int64_t(1) << 19;
+
+inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+inline int stream_tiles(int H) { return (H + kStreamTileCols - 1) / kStreamTileCols; }
+
+// Smallest chunks-per-thread that keeps a CTA within kRowsMaxThreads threads.
+inline int pick_cpt(int chunks) {
+    for (int cpt = 1; cpt <= 4; cpt *= 2)
+        if ((chunks + cpt - 1) / cpt <= kRowsMaxThreads) return cpt;
+    return 0;
+}
+
+// Cluster size for the split-H variant: the largest power of two <= cmax
+// that divides the chunk count and leaves at least one warp of chunks per CTA.
+inline int auto_cluster(int chunks, int cmax = 8) {
+    int c = cmax;
+    while (c > 1 && (chunks % c != 0 || chunks / c < 32)) c /= 2;
+    return c;
+}
+
+// Cluster size for a latency-bound call of T*H = elems (measured on GB300, a
+// CUDA graph of back-to-back calls, cold inputs, H = 4096 and 8192): up to
+// 2^14 elements the fewest CTAs that give each 128 threads (one 16-byte chunk
+// per thread: H=4096 -> 4, H=8192 -> 8; 3 % faster than 8 at H=4096, T=1);
+// up to 2^17 clusters of 16 (4-9 % faster than 8 at T = 4..32, H = 4096 and
+// T = 4..16, H = 8192); up to 2^18, 8 (16 is 7 % slower at T=32, H=8192); up
+// to 2^19 the fewest CTAs of 256 threads each (H=4096 -> 2, H=8192 -> 4: 3-5 %
+// faster than one CTA per token at H=4096, 9-18 % at H=8192).  1 = no cluster.
+inline int decode_cluster(int chunks, int64_t elems) {
+    auto split = [chunks](int threads) {
+        int c = 1;
+        while (c < 16 && chunks / (2 * c) >= threads && chunks % (2 * c) == 0) c *= 2;
+        return c;
+    };
+    if (elems <= (int64_t(1) << 14)) return split(128);
+    if (elems <= (int64_t(1) << 17)) return auto_cluster(chunks, 16);
+    if (elems <= (int64_t(1) << 18)) return auto_cluster(chunks);
+    return split(256);
+}
+
+// Persistent CTAs for T tokens on `sms` SMs: the fewest rounds of one token
+// per CTA, over as few CTAs as give every CTA the same number of tokens (+-1).
+// T = 512 on 152 SMs: 128 CTAs x 4 tokens instead of 56 CTAs with 4 and 96
+// with 3 (measured 4 % faster at H = 8192, and never slower from T = 200 to
+// T = 16384: the last round no longer runs on a fraction of the SMs).
+inline int stream_grid(int64_t T, int sms) {
+    if (T <= sms) return static_cast<int>(T > 0 ? T : 1);
+    const int64_t rounds = (T + sms - 1) / sms;
+    return static_cast<int>((T + rounds - 1) / rounds);
+}
+
+struct PolicyIn {
+    int64_t T, H;
+    int k;
+    bool fused;          // residual + RMSNorm
+    bool fp4;            // NVFP4 output
+    bool expert_norm;    // RMSNorm per expert row
+    int force_variant;   // MFR_VARIANT_*
+    int cluster_size;    // 0 = auto
+    int stages;          // ring depth the device's shared memory allows for this plan
+    int sms;
+};
+
+struct PolicyOut {
+    int variant;         // MFR_VARIANT_CLUSTER / _ROWS / _STREAM
+    int cluster;         // CTAs per token (1 = none)
+    int cpt;             // 16-byte chunks per thread per row (one-CTA kernels)
+    int block;           // threads per CTA
+    int grid_x;          // CTAs launched
+    int early_trigger;   // signal dependents at kernel entry
+};
+
+// Fills *out, or returns an MFR_ERR_* code with a reason in err.  The caller
+// has validated T, H, k and the option ranges.
+inline int choose_launch(const PolicyIn& in, PolicyOut* out, char* err, size_t errn, int ring_threads) {
+    const int chunks = static_cast<int>(in.H / 8);
+    int variant = in.force_variant;
+    int csize = in.cluster_size;
+    if (in.fp4 && in.H % 16 != 0) {
+        snprintf(err, errn, "NVFP4 output needs H %% 16 == 0 (H=%lld)", (long long)in.H);
+        return MFR_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (in.expert_norm) {
+        // one CTA per token (mfr_expert_norm.cu), or the ring kernel, which
+        // keeps a token's rows available until its slot scales are known: k <= 8,
+        // at most 4 column tiles (H <= 8192), and a ring that holds a whole
+        // token when it has more than 2 tiles
+        const int tiles = stream_tiles(static_cast<int>(in.H));
+        const bool ring_ok = in.k <= 8 && in.H <= 8192 && in.stages >= 2 && (tiles <= 2 || in.stages >= tiles);
+        if (variant == MFR_VARIANT_CLUSTER) {
+            snprintf(err, errn, "the per-expert RMSNorm finalize has no cluster variant");
+            return MFR_ERR_INVALID_ARG;
+        }
+        if (variant == MFR_VARIANT_STREAM && !ring_ok) {
+            snprintf(err, errn, "the per-expert RMSNorm ring kernel needs k <= 8 and H <= 8192");
+            return MFR_ERR_UNSUPPORTED_SHAPE;
+        }
+        if (variant == MFR_VARIANT_AUTO)
+            variant = (ring_ok && in.T * in.H >= kRowsMaxElems) ? MFR_VARIANT_STREAM : MFR_VARIANT_ROWS;
+        csize = 1;
+    }
+    if (variant == MFR_VARIANT_AUTO) {
+        const int64_t elems = in.T * in.H;
+        if (elems <= kClusterMaxElems) {
+            if (csize == 0) csize = decode_cluster(chunks, elems);
+            variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
+        } else if (elems < kRowsMaxElems || in.stages < 2) {
+            variant = MFR_VARIANT_ROWS;
+        } else {
+            variant = MFR_VARIANT_STREAM;
+        }
+    } else if (variant == MFR_VARIANT_CLUSTER) {
+        if (csize == 0) csize = auto_cluster(chunks);
+        if (csize < 2) csize = 2;
+    }
+    if (variant != MFR_VARIANT_CLUSTER) csize = 1;
+    // NVFP4 blocks of 16 columns must not straddle two CTAs of a cluster
+    while (in.fp4 && csize > 1 && (chunks / csize) % 2 != 0) csize /= 2;
+    if (variant == MFR_VARIANT_CLUSTER && csize < 2) variant = MFR_VARIANT_ROWS;
+
+    PolicyOut o{};
+    o.variant = variant;
+    // Signal dependents at kernel entry only while this grid is small: a
+    // large grid would let the next kernel park CTAs on every SM for the
+    // whole call (the ring kernel never signals early, see mfr_stream.cu).
+    o.early_trigger = (variant != MFR_VARIANT_STREAM && in.T * in.H <= kEarlyTriggerMaxElems) ? 1 : 0;
+    if (variant == MFR_VARIANT_STREAM) {
+        if (in.stages < 2) {
+            snprintf(err, errn, "k=%d leaves room for fewer than 2 ring stages", in.k);
+            return MFR_ERR_UNSUPPORTED_SHAPE;
+        }
+        o.cluster = 1;
+        o.cpt = 1;
+        o.block = ring_threads;
+        o.grid_x = stream_grid(in.T, in.sms);
+    } else {
+        if (chunks % csize != 0) {
+            snprintf(err, errn, "cluster of %d CTAs needs H/8 divisible by it (H=%lld)", csize, (long long)in.H);
+            return MFR_ERR_UNSUPPORTED_SHAPE;
+        }
+        const int cta_chunks = chunks / csize;
+        o.cluster = csize;
+        o.cpt = pick_cpt(cta_chunks);
+        if (o.cpt == 0) {
+            snprintf(err, errn, "H=%lld too wide", (long long)in.H);
+            return MFR_ERR_UNSUPPORTED_SHAPE;
+        }
+        o.block = round_up((cta_chunks + o.cpt - 1) / o.cpt, 32);
+        o.grid_x = static_cast<int>(in.T > 0 ? in.T * csize : csize);
+    }
+    *out = o;
+    return MFR_OK;
+}
+
+}  // namespace mfr

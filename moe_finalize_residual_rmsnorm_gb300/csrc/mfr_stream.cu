@@ -47,6 +47,7 @@ constexpr int kColsPT = 4;                     // columns per consumer thread an
 constexpr int kStreamNT = 512;                 // consumer threads (16 warps)
 constexpr int kStreamThreads = kStreamNT + 32; // + one producer warp
 constexpr int kStreamCB = kStreamNT * kColsPT; // columns per tile (2048)
+static_assert(kStreamCB == kStreamTileCols, "the plan policy counts tiles of kStreamTileCols columns");
 constexpr int kHeaderBytes = 128;              // per stage: weights + slot mask
 
 struct StageHeader {
@@ -528,8 +529,6 @@ StreamKernel stream_kernel_for(int H, bool fused, bool fp4, bool en) {
 }  // namespace
 
 int stream_threads() { return kStreamThreads; }
-
-int stream_tiles(int H) { return (H + kStreamCB - 1) / kStreamCB; }
 
 int stream_stage_bytes(int k, bool fused) {
     return kHeaderBytes + k * kStreamCB * 2 + (fused ? kStreamCB * 4 : 0);

@@ -1,0 +1,154 @@
+"""The plan's launch policy (csrc/mfr_policy.h) on the CPU: which kernel,
+how many CTAs per token, threads and grid for a call of T tokens of width H.
+
+The header is pure host C++; this test compiles it into a small shared
+library with the host compiler and checks the choices the design notes
+state, the edges of every threshold, the even spread of the persistent
+grid, and the refusals."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import moe_finalize_residual_rmsnorm_gb300 as mfr
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(ROOT, "moe_finalize_residual_rmsnorm_gb300", "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+SMS = 152
+RING_THREADS = 544
+ERR_ARG, ERR_SHAPE = 1, 2      # MFR_ERR_INVALID_ARG, MFR_ERR_UNSUPPORTED_SHAPE
+
+SHIM = r'''
+#include "mfr_policy.h"
+extern "C" int policy_choose(long long T, long long H, int k, int fused, int fp4, int en, int fv, int cs,
+                             int stages, int sms, int* out, char* err, int errn) {
+    mfr::PolicyIn in{T, H, k, fused != 0, fp4 != 0, en != 0, fv, cs, stages, sms};
+    mfr::PolicyOut o{};
+    const int rc = mfr::choose_launch(in, &o, err, static_cast<size_t>(errn), 544);
+    out[0] = o.variant; out[1] = o.cluster; out[2] = o.cpt; out[3] = o.block; out[4] = o.grid_x;
+    out[5] = o.early_trigger;
+    return rc;
+}
+extern "C" int policy_stream_grid(long long T, int sms) { return mfr::stream_grid(T, sms); }
+'''
+
+
+@pytest.fixture(scope="module")
+def lib(tmp_path_factory):
+    d = tmp_path_factory.mktemp("policy")
+    src = d / "shim.cpp"
+    src.write_text(SHIM)
+    so = d / "libpolicy.so"
+    subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", f"-I{CSRC}", f"-I{INCLUDE}", str(src),
+                    "-o", str(so)], check=True)
+    L = ctypes.CDLL(str(so))
+    L.policy_choose.restype = ctypes.c_int
+    L.policy_choose.argtypes = [ctypes.c_longlong, ctypes.c_longlong] + [ctypes.c_int] * 8 + \
+        [ctypes.POINTER(ctypes.c_int), ctypes.c_char_p, ctypes.c_int]
+    L.policy_stream_grid.restype = ctypes.c_int
+    L.policy_stream_grid.argtypes = [ctypes.c_longlong, ctypes.c_int]
+    return L
+
+
+def choose(lib, T, H, k=8, fused=True, fp4=False, en=False, variant=mfr.VARIANT_AUTO, cluster=0, stages=5):
+    out = (ctypes.c_int * 6)()
+    err = ctypes.create_string_buffer(200)
+    rc = lib.policy_choose(T, H, k, int(fused), int(fp4), int(en), variant, cluster, stages, SMS, out, err, 200)
+    keys = ("variant", "cluster", "cpt", "block", "grid_x", "early_trigger")
+    return rc, dict(zip(keys, list(out))), err.value.decode()
+
+
+AUTO_TABLE = [
+    # (T, H, variant, CTAs per token)
+    (1, 4096, mfr.VARIANT_CLUSTER, 4), (4, 4096, mfr.VARIANT_CLUSTER, 4), (5, 4096, mfr.VARIANT_CLUSTER, 16),
+    (8, 4096, mfr.VARIANT_CLUSTER, 16), (32, 4096, mfr.VARIANT_CLUSTER, 16), (33, 4096, mfr.VARIANT_CLUSTER, 8),
+    (64, 4096, mfr.VARIANT_CLUSTER, 8), (65, 4096, mfr.VARIANT_CLUSTER, 2), (128, 4096, mfr.VARIANT_CLUSTER, 2),
+    (129, 4096, mfr.VARIANT_ROWS, 1), (383, 4096, mfr.VARIANT_ROWS, 1), (384, 4096, mfr.VARIANT_STREAM, 1),
+    (16384, 4096, mfr.VARIANT_STREAM, 1),
+    (1, 8192, mfr.VARIANT_CLUSTER, 8), (2, 8192, mfr.VARIANT_CLUSTER, 8), (3, 8192, mfr.VARIANT_CLUSTER, 16),
+    (16, 8192, mfr.VARIANT_CLUSTER, 16), (32, 8192, mfr.VARIANT_CLUSTER, 8), (64, 8192, mfr.VARIANT_CLUSTER, 4),
+    (65, 8192, mfr.VARIANT_ROWS, 1), (191, 8192, mfr.VARIANT_ROWS, 1), (192, 8192, mfr.VARIANT_STREAM, 1),
+    (2, 1024, mfr.VARIANT_ROWS, 1), (32, 1024, mfr.VARIANT_CLUSTER, 4), (1, 16384, mfr.VARIANT_CLUSTER, 16),
+]
+
+
+@pytest.mark.parametrize("T,H,variant,cluster", AUTO_TABLE)
+def test_automatic_choice(lib, T, H, variant, cluster):
+    rc, o, _ = choose(lib, T, H)
+    assert rc == mfr.MFR_OK
+    assert (o["variant"], o["cluster"]) == (variant, cluster)
+    if variant == mfr.VARIANT_STREAM:
+        assert o["block"] == RING_THREADS and o["early_trigger"] == 0
+    else:
+        assert o["grid_x"] == T * cluster
+        assert o["early_trigger"] == (1 if T * H <= 1 << 19 else 0)
+        chunks = H // 8 // cluster
+        assert o["cpt"] * o["block"] >= chunks and o["block"] % 32 == 0 and o["block"] <= 512
+
+
+def test_one_cta_geometry(lib):
+    for H, cpt, block in ((24, 1, 32), (4096, 1, 512), (4104, 2, 288), (8192, 2, 512), (16384, 4, 512)):
+        rc, o, _ = choose(lib, 300, H, variant=mfr.VARIANT_ROWS)
+        assert rc == 0 and (o["cpt"], o["block"], o["grid_x"]) == (cpt, block, 300), H
+
+
+def test_persistent_grid_spreads_tokens_evenly(lib):
+    for T in range(1, 5001):
+        g = lib.policy_stream_grid(T, SMS)
+        rounds = -(-T // SMS)
+        assert 1 <= g <= SMS
+        assert -(-T // g) == rounds                      # no extra round
+        loads = [len(range(b, T, g)) for b in range(g)]
+        assert max(loads) - min(loads) <= 1              # every CTA within one token of the others
+        assert g == T or g == -(-T // rounds)            # as few CTAs as that allows
+
+
+def test_forced_variants_and_cluster_sizes(lib):
+    rc, o, _ = choose(lib, 16, 4096, variant=mfr.VARIANT_CLUSTER, cluster=2)
+    assert rc == 0 and (o["variant"], o["cluster"], o["block"]) == (mfr.VARIANT_CLUSTER, 2, 256)
+    rc, o, _ = choose(lib, 16, 4096, variant=mfr.VARIANT_CLUSTER)            # auto size when forced
+    assert rc == 0 and o["cluster"] == 8
+    rc, o, _ = choose(lib, 16, 32, variant=mfr.VARIANT_CLUSTER)              # narrow: still split in 2
+    assert rc == 0 and (o["variant"], o["cluster"], o["block"]) == (mfr.VARIANT_CLUSTER, 2, 32)
+    for H in (24, 4104):                                                      # 3 and 513 chunks
+        rc, o, err = choose(lib, 16, H, variant=mfr.VARIANT_CLUSTER, cluster=2)
+        assert rc == ERR_SHAPE and "divisible" in err
+    rc, o, _ = choose(lib, 5, 4096, variant=mfr.VARIANT_STREAM)
+    assert rc == 0 and o["variant"] == mfr.VARIANT_STREAM and o["grid_x"] == 5
+    rc, _, err = choose(lib, 500, 4096, variant=mfr.VARIANT_STREAM, stages=1)
+    assert rc == ERR_SHAPE and "stages" in err
+    rc, o, _ = choose(lib, 5000, 4096, stages=1)                              # no ring room: one CTA per token
+    assert rc == 0 and o["variant"] == mfr.VARIANT_ROWS
+
+
+def test_nvfp4_rules(lib):
+    rc, _, err = choose(lib, 4, 4104, fp4=True)
+    assert rc == ERR_SHAPE and "16" in err
+    # blocks of 16 columns never straddle two CTAs: 514 chunks split in 2 gives 257, odd
+    rc, o, _ = choose(lib, 4, 4112, fp4=True, variant=mfr.VARIANT_CLUSTER, cluster=2)
+    assert rc == 0 and o["variant"] == mfr.VARIANT_ROWS and o["cluster"] == 1
+    rc, o, _ = choose(lib, 1, 4096, fp4=True)
+    assert rc == 0 and o["cluster"] == 4
+
+
+def test_per_expert_rmsnorm_rules(lib):
+    ok = dict(fused=False, en=True, stages=7)
+    rc, o, _ = choose(lib, 16384, 4096, **ok)
+    assert rc == 0 and o["variant"] == mfr.VARIANT_STREAM
+    rc, o, _ = choose(lib, 256, 4096, **ok)
+    assert rc == 0 and (o["variant"], o["cluster"]) == (mfr.VARIANT_ROWS, 1)
+    rc, o, _ = choose(lib, 1, 4096, **ok)                                      # never a cluster
+    assert rc == 0 and (o["variant"], o["cluster"]) == (mfr.VARIANT_ROWS, 1)
+    rc, o, _ = choose(lib, 16384, 4096, k=16, fused=False, en=True, stages=3)
+    assert rc == 0 and o["variant"] == mfr.VARIANT_ROWS                      # more than 8 slots
+    rc, _, _ = choose(lib, 16384, 4096, k=16, fused=False, en=True, stages=3, variant=mfr.VARIANT_STREAM)
+    assert rc == ERR_SHAPE
+    rc, _, _ = choose(lib, 64, 16384, fused=False, en=True, stages=7, variant=mfr.VARIANT_STREAM)
+    assert rc == ERR_SHAPE                                                     # more than 4 tiles
+    rc, _, _ = choose(lib, 16384, 8192, fused=False, en=True, stages=3, variant=mfr.VARIANT_STREAM)
+    assert rc == ERR_SHAPE                                                     # ring cannot hold a token
+    rc, _, _ = choose(lib, 64, 4096, fused=False, en=True, stages=7, variant=mfr.VARIANT_CLUSTER)
+    assert rc == ERR_ARG
