@@ -112,11 +112,10 @@ inline int choose_launch(const PolicyIn& in, PolicyOut* out, char* err, size_t e
     }
     if (in.expert_norm) {
         // one CTA per token (mfr_expert_norm.cu), or the ring kernel, which
-        // keeps a token's rows available until its slot scales are known: k <= 8,
-        // at most 4 column tiles (H <= 8192), and a ring that holds a whole
-        // token when it has more than 2 tiles
-        const int tiles = stream_tiles(static_cast<int>(in.H));
-        const bool ring_ok = in.k <= 8 && in.H <= 8192 && in.stages >= 2 && (tiles <= 2 || in.stages >= tiles);
+        // keeps a token's rows available until its slot scales are known: k <= 8
+        // and at most 4 column tiles (H <= 8192); two tiles sit in registers and
+        // at most two stages are held, so two ring stages suffice
+        const bool ring_ok = in.k <= 8 && in.H <= 8192 && in.stages >= 2;
         if (variant == MFR_VARIANT_CLUSTER) {
             snprintf(err, errn, "the per-expert RMSNorm finalize has no cluster variant");
             return MFR_ERR_INVALID_ARG;

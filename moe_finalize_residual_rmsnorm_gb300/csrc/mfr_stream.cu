@@ -19,7 +19,8 @@
 // With EN = true (FUSED = false, k <= 8, at most 4 tiles) it is the finalize
 // with an RMSNorm per expert row, the reading of the PR 6544 analysis, section
 // 2.1 (see mfr_expert_norm.cu): each consumer thread keeps its four columns
-// of every slot and tile packed in registers while it sums each slot's
+// of every slot of the first two tiles packed in registers (later tiles stay
+// in their ring stages until the second pass) while it sums each slot's
 // squares (bf16 operands straight into the FMA), the CTA reduces the k sums
 // (a reduce-scatter butterfly in each warp, then thread j adds slot j over
 // the warps in index order), c_j = w_j * rsqrt(ss_j / H + eps), and
@@ -228,17 +229,18 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
     uint32_t phase = 0;
     if constexpr (EN) {
         // ---- RMSNorm per expert row: the rows stay available until the token's c_j are known.
-        // With at most 2 tiles a thread keeps its share of them packed in
-        // registers and releases each stage at once; with more (H > 4096) the
-        // stages themselves are held until the second pass re-reads them, so
-        // no registers hold rows (a token's tiles fit in the ring: the plan
-        // checks stages >= tiles) and the producer refills only the stages
-        // left over.  Measured at H = 8192: holding stages is faster than 64
-        // registers of packed rows.
-        constexpr bool kHold = MAXTILES > 2;
+        // A thread keeps its share of the first kRegTiles tiles packed in
+        // registers (32 registers) and releases those stages at once; the
+        // stages of later tiles (H > 4096) are held until the second pass
+        // re-reads them, and the producer refills the stages left over.  At
+        // most MAXTILES - kRegTiles = 2 stages are held, so a ring of 2 stages
+        // never deadlocks.  Measured at H = 8192, T = 4096: 91.4 us, against
+        // 99.1 us holding all four stages (and slower still with all four
+        // tiles in 64 registers).
+        constexpr int kRegTiles = 2;
         const int lane = tid & 31;
         for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
-            uint2 rv[kHold ? 1 : MAXTILES][kHold ? 1 : 8];
+            uint2 rv[kRegTiles][8];
             float ss[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) ss[j] = 0.f;
@@ -265,16 +267,18 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 if (tid < 8) my_w = hd->w[tid];
                 const int c0 = b * kStreamCB;
                 const bool mine = tid * kColsPT < min(kStreamCB, H - c0);
+                const bool in_regs = b < kRegTiles;       // a constant: the loop is unrolled
+                const int rb = in_regs ? b : 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    if constexpr (!kHold) rv[b][j] = make_uint2(0, 0);
+                    if (in_regs) rv[rb][j] = make_uint2(0, 0);
                     if (j < k && (mask & (1u << j)) && mine) {
                         const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
-                        if constexpr (!kHold) rv[b][j] = v;
+                        if (in_regs) rv[rb][j] = v;
                         ss[j] = sumsq_bf16x4(v, ss[j]);   // bf16 operands straight into the FMA
                     }
                 }
-                if constexpr (!kHold) {
+                if (in_regs) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(ebar);     // this warp is done with the stage
                 }
@@ -332,6 +336,8 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 const unsigned char* st = stages + static_cast<size_t>(s2) * stage_bytes;
                 const uint32_t ebar = smem_u32(&bars[nstages + s2]);
                 if (++s2 == nstages) { s2 = 0; phase2 ^= 1u; }
+                const bool in_regs = b < kRegTiles;
+                const int rb = in_regs ? b : 0;
                 float acc[kColsPT];
 #pragma unroll
                 for (int q = 0; q < kColsPT; ++q) acc[q] = 0.f;
@@ -340,15 +346,15 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                     for (int j = 0; j < 8; ++j) {
                         if (j < k && (mask & (1u << j))) {
                             uint2 v;
-                            if constexpr (kHold) v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
-                            else v = rv[b][j];
+                            if (in_regs) v = rv[rb][j];
+                            else v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
                             const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
 #pragma unroll
                             for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(cr[j], e[q], acc[q]);
                         }
                     }
                 }
-                if constexpr (kHold) {
+                if (!in_regs) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(ebar);     // both passes are done with the stage
                 }

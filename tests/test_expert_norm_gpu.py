@@ -57,7 +57,8 @@ def assert_expert_norm_close(got_bits, want_bits, y, s):
 
 
 @pytest.mark.parametrize("T,H,k", [(1, 4096, 8), (5, 24, 3), (16, 4096, 8), (100, 8192, 8), (7, 4104, 16),
-                                   (153, 1032, 1), (3, 16384, 8), (9, 8, 5), (160, 4104, 5), (305, 2048, 8)])
+                                   (153, 1032, 1), (3, 16384, 8), (9, 8, 5), (160, 4104, 5), (305, 2048, 8),
+                                   (40, 6144, 8), (20, 8000, 6)])
 @pytest.mark.parametrize("variant", [mfr.VARIANT_AUTO, mfr.VARIANT_ROWS, mfr.VARIANT_STREAM],
                          ids=["auto", "rows", "ring"])
 @pytest.mark.parametrize("pdl", [True, False])

@@ -148,7 +148,11 @@ def test_per_expert_rmsnorm_rules(lib):
     assert rc == ERR_SHAPE
     rc, _, _ = choose(lib, 64, 16384, fused=False, en=True, stages=7, variant=mfr.VARIANT_STREAM)
     assert rc == ERR_SHAPE                                                     # more than 4 tiles
-    rc, _, _ = choose(lib, 16384, 8192, fused=False, en=True, stages=3, variant=mfr.VARIANT_STREAM)
-    assert rc == ERR_SHAPE                                                     # ring cannot hold a token
+    rc, o, _ = choose(lib, 16384, 8192, fused=False, en=True, stages=2, variant=mfr.VARIANT_STREAM)
+    assert rc == 0 and o["variant"] == mfr.VARIANT_STREAM                    # two stages are enough
+    rc, o, _ = choose(lib, 16384, 8192, fused=False, en=True, stages=1)
+    assert rc == 0 and o["variant"] == mfr.VARIANT_ROWS
+    rc, _, _ = choose(lib, 16384, 8192, fused=False, en=True, stages=1, variant=mfr.VARIANT_STREAM)
+    assert rc == ERR_SHAPE
     rc, _, _ = choose(lib, 64, 4096, fused=False, en=True, stages=7, variant=mfr.VARIANT_CLUSTER)
     assert rc == ERR_ARG
