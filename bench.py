@@ -271,9 +271,14 @@ def cpu_baseline(inp_host, wl, target_s: float):
     n_tokens = calibrate_tokens(inp_host, wl.T, target_s, cores)
     dt, n = time_oracle(inp_host, n_tokens, cores, 2)
     gbs = W.algorithmic_bytes(n, wl.H, wl.k) / dt / 1e9
+    # the same code on one thread, on a quarter of one thread's share of the sample
+    dt1, n1 = time_oracle(inp_host, max(1, n // (4 * cores)), 1, 3)
+    gbs1 = W.algorithmic_bytes(n1, wl.H, wl.k) / dt1 / 1e9
     return {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} tokens drawn from the {wl.T}-token workload (seeded; whole shuffled passes "
-                      f"when more than {wl.T}), H={wl.H}, k={wl.k}, {dt:.2f} s wall, {cores} host threads"}
+                      f"when more than {wl.T}), H={wl.H}, k={wl.k}, {dt:.2f} s wall, {cores} host threads",
+            "single_thread": {"value": round(gbs1, 4), "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} tokens, {dt1:.2f} s wall, 1 host thread"}}
 
 
 # --- the GPU arm -------------------------------------------------------------------------
