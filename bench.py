@@ -425,12 +425,20 @@ def run_e2e(args, plan, dev, nbytes, world, dist, device):
 
 def run_sweep(mfr, device, args):
     """µs/call and GB/s at each decode and wide size, with the plan the
-    library picks.  Calls are captured in a CUDA graph (a decode call is far
-    shorter than a Python launch), cycling through enough input/output sets
-    that together exceed 3x L2, so each call reads cold data.  The floor is
-    the same graph of empty kernels with the identical launch geometry
-    (moe_finalize_rmsnorm_launch_floor); the decode target is
-    us_per_call <= 2 * (floor + bytes / 8 TB/s)."""
+    library picks, three ways:
+      us_per_call  calls captured in a CUDA graph (a decode call is far
+                   shorter than a Python launch), cycling through enough
+                   input/output sets that together exceed 3x L2, so each call
+                   reads cold data; median of 5 replays.  Graphs of small calls
+                   hold 4096 calls, so every size is timed at the same
+                   steady state.
+      loop_us      the same calls launched one by one from Python through the C
+                   ABI (pointers taken once), CUDA events around 200+ calls,
+                   median of 5 batches (host-bound for small calls: context only).
+      warm_us      the graph over a single input set (inputs in L2; context only).
+    The floor is the same graph (or loop) of empty kernels with the identical
+    launch geometry and PDL attribute (moe_finalize_rmsnorm_launch_floor);
+    the decode target is us_per_call <= 2 * (floor_us + bytes / 8 TB/s)."""
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     rows = []
     for wl in [W.decode(t) for t in W.DECODE_TOKENS] + [W.wide(t) for t in W.WIDE_TOKENS]:
@@ -447,40 +455,76 @@ def run_sweep(mfr, device, args):
         g = base["gamma"]
         plan = mfr.Plan(T, H, k, R, enable_pdl=not args.no_pdl)
         stream = torch.cuda.Stream(device)
-        ncalls = max(nsets, 64 if T <= 512 else 8)
+        ncalls = max(nsets, 4096 if nbytes <= (16 << 20) else 64)
 
-        def capture(floor: bool):
+        def launch(i, floor, sets):
+            if floor:
+                plan.launch_floor(stream)
+            else:
+                j = i % sets
+                plan.run(E[j], idx[j], w[j], res[j], rout[j], g, base["eps"], out[j], stream, validate=False)
+
+        def graph_us(floor: bool, sets: int, reps=5):
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 for i in range(ncalls):
-                    j = i % nsets
-                    if floor:
-                        plan.launch_floor(stream)
-                    else:
-                        plan.run(E[j], idx[j], w[j], res[j], rout[j], g, base["eps"], out[j], stream,
-                                 validate=False)
-            return graph
-
-        def time_graph(graph, reps=5):
+                    launch(i, floor, sets)
             graph.replay()
             stream.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
+            times = []
             for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
                 graph.replay()
-            b.record(stream)
-            b.synchronize()
-            return a.elapsed_time(b) * 1e3 / (reps * ncalls)
+                b.record(stream)
+                b.synchronize()
+                times.append(a.elapsed_time(b) * 1e3 / ncalls)
+            del graph
+            return float(np.median(times))
+
+        # the stream loop goes through the C ABI with pointers taken once, so
+        # it times the library's host path and the launch, not tensor indexing
+        ptrs = [(E[j].data_ptr(), idx[j].data_ptr(), w[j].data_ptr(), res[j].data_ptr(), rout[j].data_ptr(),
+                 g.data_ptr(), base["eps"], out[j].data_ptr(), stream.cuda_stream) for j in range(nsets)]
+
+        def loop_us(floor: bool, batches=5):
+            n = max(200, min(ncalls, 1000))
+            run_ptrs, floor_fn, sh = plan.run_ptrs, plan.launch_floor, stream
+
+            def batch():
+                bad = 0
+                for i in range(n):
+                    if floor:
+                        floor_fn(sh)
+                    else:
+                        bad |= run_ptrs(*ptrs[i % nsets])
+                if bad:
+                    raise RuntimeError(f"moe_finalize_rmsnorm_run failed during {wl.name}")
+            batch()
+            stream.synchronize()
+            times = []
+            for _ in range(batches):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                batch()
+                b.record(stream)
+                b.synchronize()
+                times.append(a.elapsed_time(b) * 1e3 / n)
+            return float(np.median(times))
 
         with torch.cuda.stream(stream):
-            us = time_graph(capture(False))
-            floor_us = time_graph(capture(True))
+            us = graph_us(False, nsets)
+            floor_us = graph_us(True, nsets)
+            warm = graph_us(False, 1)
+            loop = loop_us(False)
+            loop_floor = loop_us(True)
         info = plan.info()
         target = 2 * (floor_us + nbytes / 8e12 * 1e6)
         rows.append({"workload": wl.name, "T": T, "H": H, "us_per_call": round(us, 3),
                      "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1), "floor_us": round(floor_us, 3),
                      "vs_2x_floor": round(us / target, 3), "variant": info["variant_name"],
-                     "cluster": info["cluster"], "sets": nsets})
+                     "cluster": info["cluster"], "sets": nsets, "graph_calls": ncalls,
+                     "warm_us": round(warm, 3), "loop_us": round(loop, 3), "loop_floor_us": round(loop_floor, 3)})
         if plan.get_status(stream) != 0:
             raise RuntimeError(f"the device status word reported an error during {wl.name}")
         del E, idx, w, res, rout, out, base

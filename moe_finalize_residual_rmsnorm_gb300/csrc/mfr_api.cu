@@ -124,8 +124,8 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
                     dev, major, minor);
 
     // ring depth the bulk-copy kernel would get on this device: room is left
-    // for the ring kernel's static shared memory (640 bytes in its per-expert
-    // RMSNorm mode, the largest) and slack
+    // for the ring kernel's static shared memory (at most 1152 bytes, in its
+    // NVFP4 form: the encode-scale table) and slack
     const int ring_budget = smem_optin - 2048;
     int stages = 0;
     while (stages < mfr::kMaxStages && mfr::stream_smem_bytes(k, stages + 1, fused) <= ring_budget) ++stages;
