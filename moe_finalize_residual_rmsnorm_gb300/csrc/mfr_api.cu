@@ -165,26 +165,48 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         // grid take more waves of resident CTAs (512-thread CTAs fit twice
         // per SM without them, once with them).
         l.regslots = 1;
-        if (!expert_norm) {   // that kernel always holds them in registers
+        auto waves = [&](int per_sm) -> int64_t {
+            const int64_t slots = static_cast<int64_t>(per_sm) * sms;
+            return slots > 0 ? (l.grid_x + slots - 1) / slots : INT64_MAX;
+        };
+        if (expert_norm) {
+            // The one-pass form holds up to 8 rows of at most 2 chunks per
+            // thread; one CTA per token takes the two-pass form instead where
+            // the one-pass form's registers would add a wave of CTAs.
+            l.regslots = mfr::expert_norm_one_pass(k, l.cpt) ? 1 : 0;
+            if (l.regslots && l.cluster == 1) {
+                int one = 0, two = 0;
+                if ((e = mfr::expert_norm_blocks_per_sm(l, true, &one)) != cudaSuccess ||
+                    (e = mfr::expert_norm_blocks_per_sm(l, false, &two)) != cudaSuccess) {
+                    cudaGetLastError();
+                    return fail_cuda(MFR_ERR_CUDA, "occupancy query", e);
+                }
+                if (two > 0 && waves(two) < waves(one)) l.regslots = 0;
+            }
+            if (l.cluster > 1 && !l.regslots)
+                return fail(MFR_ERR_UNSUPPORTED_SHAPE, "no per-expert RMSNorm cluster form for k=%d, H=%lld",
+                            k, (long long)H);
+            if ((e = mfr::expert_norm_prepare(l)) != cudaSuccess) {
+                cudaGetLastError();
+                return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
+            }
+        } else {
             int with_regs = 0, without = 0;
             if ((e = mfr::rows_blocks_per_sm(l, true, &with_regs)) != cudaSuccess ||
                 (e = mfr::rows_blocks_per_sm(l, false, &without)) != cudaSuccess) {
                 cudaGetLastError();
                 return fail_cuda(MFR_ERR_CUDA, "occupancy query", e);
             }
-            auto waves = [&](int per_sm) -> int64_t {
-                const int64_t slots = static_cast<int64_t>(per_sm) * sms;
-                return slots > 0 ? (l.grid_x + slots - 1) / slots : INT64_MAX;
-            };
             if (without > 0 && waves(without) < waves(with_regs)) l.regslots = 0;
         }
         if (!expert_norm && (e = mfr::rows_prepare(l)) != cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }
-        if (l.cluster > 1 && fused) {
+        if (l.cluster > 1 && (fused || expert_norm)) {
             int nclusters = 0;
-            e = mfr::rows_max_active_clusters(l, &nclusters);
+            e = expert_norm ? mfr::expert_norm_max_active_clusters(l, &nclusters)
+                            : mfr::rows_max_active_clusters(l, &nclusters);
             if (e != cudaSuccess || nclusters < 1) {
                 cudaGetLastError();
                 return fail(MFR_ERR_UNSUPPORTED_SHAPE, "a cluster of %d CTAs x %d threads cannot be resident",

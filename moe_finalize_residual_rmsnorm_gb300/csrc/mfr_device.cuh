@@ -230,4 +230,30 @@ __device__ __forceinline__ float warp_allreduce_sum(float v) {
     return v;
 }
 
+// Per-slot sums of 8 values over a warp in 9 shuffles: a reduce-scatter
+// butterfly (xor 16, 8, 4 halve the slots a lane carries; xor 2, 1 finish)
+// that returns the warp's sum of slot (lane >> 2) & 7 in lanes 4m..4m+3.
+// The order of the additions is fixed, so the result is reproducible.
+__device__ __forceinline__ float warp_reduce_scatter8(const float (&ss)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b4 ? ss[i] : ss[i + 4];
+        const float keep = b4 ? ss[i + 4] : ss[i];
+        a[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    }
+    float b[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b3 ? a[i] : a[i + 2];
+        const float keep = b3 ? a[i + 2] : a[i];
+        b[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    }
+    float c = (b2 ? b[1] : b[0]) + __shfl_xor_sync(0xFFFFFFFFu, b2 ? b[0] : b[1], 4);
+    c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
+    c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
+    return c;
+}
+
 }  // namespace mfr

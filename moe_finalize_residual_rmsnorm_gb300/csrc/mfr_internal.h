@@ -62,8 +62,15 @@ cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s);
 // An empty kernel with the plan's launch geometry (for the launch floor).
 cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s);
 
-// mfr_expert_norm.cu: one CTA per token, each expert row RMS-normalised
-// before the weighted sum.  Launch uses grid_x (tokens), block, cpt, pdl.
+// mfr_expert_norm.cu: each expert row RMS-normalised before the weighted
+// sum.  With regslots the one-pass kernel (k <= 8, cpt <= 2; a cluster of
+// `cluster` CTAs per token when cluster > 1), else the two-pass kernel (one
+// CTA per token).  Launch uses grid_x, block, cluster, cpt, pdl, regslots.
+bool expert_norm_one_pass(int k, int cpt);
+cudaError_t expert_norm_prepare(const Launch& l);   // checks the form; cluster > 8 attribute
+// Resident CTAs per SM of the one-pass or the two-pass kernel for l's cpt and block.
+cudaError_t expert_norm_blocks_per_sm(const Launch& l, bool one_pass, int* n);
+cudaError_t expert_norm_max_active_clusters(const Launch& l, int* n);
 cudaError_t expert_norm_launch(const Params& p, const Launch& l, cudaStream_t s);
 
 // mfr_stream.cu: persistent CTAs fed by bulk copies into a shared-memory ring.

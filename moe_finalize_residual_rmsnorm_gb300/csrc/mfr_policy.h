@@ -111,22 +111,31 @@ inline int choose_launch(const PolicyIn& in, PolicyOut* out, char* err, size_t e
         return MFR_ERR_UNSUPPORTED_SHAPE;
     }
     if (in.expert_norm) {
-        // one CTA per token (mfr_expert_norm.cu), or the ring kernel, which
-        // keeps a token's rows available until its slot scales are known: k <= 8
-        // and at most 4 column tiles (H <= 8192); two tiles sit in registers and
-        // at most two stages are held, so two ring stages suffice
+        // mfr_expert_norm.cu: a cluster of CTAs per token (small calls) or one
+        // CTA per token, both holding the rows in registers when k <= 8; or the
+        // ring kernel, which keeps a token's rows available until its slot
+        // scales are known: k <= 8 and at most 4 column tiles (H <= 8192); two
+        // tiles sit in registers and at most two stages are held, so two ring
+        // stages suffice.  The cluster sizes are those of the fused kernel.
         const bool ring_ok = in.k <= 8 && in.H <= 8192 && in.stages >= 2;
-        if (variant == MFR_VARIANT_CLUSTER) {
-            snprintf(err, errn, "the per-expert RMSNorm finalize has no cluster variant");
-            return MFR_ERR_INVALID_ARG;
+        const bool regs_ok = in.k <= 8;
+        if (variant == MFR_VARIANT_CLUSTER && !regs_ok) {
+            snprintf(err, errn, "the per-expert RMSNorm cluster form holds at most 8 slots (k=%d)", in.k);
+            return MFR_ERR_UNSUPPORTED_SHAPE;
         }
         if (variant == MFR_VARIANT_STREAM && !ring_ok) {
             snprintf(err, errn, "the per-expert RMSNorm ring kernel needs k <= 8 and H <= 8192");
             return MFR_ERR_UNSUPPORTED_SHAPE;
         }
-        if (variant == MFR_VARIANT_AUTO)
-            variant = (ring_ok && in.T * in.H >= kRowsMaxElems) ? MFR_VARIANT_STREAM : MFR_VARIANT_ROWS;
-        csize = 1;
+        if (variant == MFR_VARIANT_AUTO) {
+            const int64_t elems = in.T * in.H;
+            if (regs_ok && elems <= kClusterMaxElems) {
+                if (csize == 0) csize = decode_cluster(chunks, elems);
+                variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
+            } else {
+                variant = (ring_ok && elems >= kRowsMaxElems) ? MFR_VARIANT_STREAM : MFR_VARIANT_ROWS;
+            }
+        }
     }
     if (variant == MFR_VARIANT_AUTO) {
         const int64_t elems = in.T * in.H;

@@ -334,7 +334,7 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attrs, const Laun
     cfg.dynamicSmemBytes = static_cast<size_t>(l.smem_bytes);
     cfg.stream = s;
     int n = 0;
-    if (l.cluster > 1 && l.fused) {
+    if (l.cluster > 1 && (l.fused || l.expert_norm)) {   // the plain finalize splits H without a cluster
         attrs[n].id = cudaLaunchAttributeClusterDimension;
         attrs[n].val.clusterDim.x = static_cast<unsigned>(l.cluster);
         attrs[n].val.clusterDim.y = 1;

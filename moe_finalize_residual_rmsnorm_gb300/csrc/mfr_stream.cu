@@ -283,30 +283,11 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                     if (lane == 0) mbar_arrive(ebar);     // this warp is done with the stage
                 }
             }
-            // Per-slot sums over the CTA in a fixed order.  In the warp, a
-            // reduce-scatter butterfly (xor 16, 8, 4 halve the slots a lane
-            // carries; xor 2, 1 finish: 9 shuffles for 8 slots) leaves the
-            // warp's sum of slot (lane >> 2) & 7 in lanes 4m..4m+3; then
+            // Per-slot sums over the CTA in a fixed order: the warp's sums by
+            // a reduce-scatter butterfly (slot m in lanes 4m..4m+3), then
             // thread j < k adds slot j over the warps in index order.
             {
-                const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-                float a[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float send = b4 ? ss[i] : ss[i + 4];
-                    const float keep = b4 ? ss[i + 4] : ss[i];
-                    a[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
-                }
-                float b_[2];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const float send = b3 ? a[i] : a[i + 2];
-                    const float keep = b3 ? a[i + 2] : a[i];
-                    b_[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
-                }
-                float c = (b2 ? b_[1] : b_[0]) + __shfl_xor_sync(0xFFFFFFFFu, b2 ? b_[0] : b_[1], 4);
-                c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
-                c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
+                const float c = warp_reduce_scatter8(ss, lane);
                 if ((lane & 3) == 0) s_slot[warp][lane >> 2] = c;
             }
             const uint32_t stop_in = (!ok || s_abort != 0) ? 1u : 0u;

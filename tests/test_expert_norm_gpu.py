@@ -59,12 +59,14 @@ def assert_expert_norm_close(got_bits, want_bits, y, s):
 @pytest.mark.parametrize("T,H,k", [(1, 4096, 8), (5, 24, 3), (16, 4096, 8), (100, 8192, 8), (7, 4104, 16),
                                    (153, 1032, 1), (3, 16384, 8), (9, 8, 5), (160, 4104, 5), (305, 2048, 8),
                                    (40, 6144, 8), (20, 8000, 6)])
-@pytest.mark.parametrize("variant", [mfr.VARIANT_AUTO, mfr.VARIANT_ROWS, mfr.VARIANT_STREAM],
-                         ids=["auto", "rows", "ring"])
+@pytest.mark.parametrize("variant", [mfr.VARIANT_AUTO, mfr.VARIANT_ROWS, mfr.VARIANT_STREAM, mfr.VARIANT_CLUSTER],
+                         ids=["auto", "rows", "ring", "cluster"])
 @pytest.mark.parametrize("pdl", [True, False])
 def test_expert_norm_matches_oracle(T, H, k, variant, pdl):
     if variant == mfr.VARIANT_STREAM and (k > 8 or H > 8192):
         pytest.skip("the ring form holds at most 8 slots and 4 column tiles")
+    if variant == mfr.VARIANT_CLUSTER and (k > 8 or (H // 8) % 2):
+        pytest.skip("the cluster form holds at most 8 slots and splits H/8 evenly")
     wl = W.Workload(f"en_T{T}_H{H}", T=T, H=H, k=k, E=max(16, 2 * k), seed=T * 11 + H + k, extra_rows=3)
     inp = W.make_inputs(wl, "cuda")
     want, y, s, bad = oracle_expert_norm(inp)
@@ -74,8 +76,37 @@ def test_expert_norm_matches_oracle(T, H, k, variant, pdl):
     assert np.mean(got != want) < 0.02
     assert plan.get_status() == 0
     info = plan.info()
-    assert info["cluster"] == 1
-    assert info["variant"] == (mfr.VARIANT_ROWS if variant == mfr.VARIANT_AUTO else variant)
+    if variant == mfr.VARIANT_AUTO:
+        small = k <= 8 and T * H <= 1 << 19
+        assert info["variant"] in ((mfr.VARIANT_CLUSTER, mfr.VARIANT_ROWS) if small else (mfr.VARIANT_ROWS,))
+    else:
+        assert info["variant"] == variant
+    assert (info["cluster"] > 1) == (info["variant"] == mfr.VARIANT_CLUSTER)
+    again, _ = run_expert_norm(inp, plan=plan)
+    assert np.array_equal(got, again)
+
+
+@pytest.mark.parametrize("T,H", [(1, 4096), (3, 8192), (16, 4096), (64, 8192)])
+@pytest.mark.parametrize("cluster", [2, 4, 8, 16])
+def test_expert_norm_every_cluster_size(T, H, cluster):
+    """The cluster form at every cluster size, against the oracle."""
+    wl = W.Workload(f"en_c{cluster}_T{T}_H{H}", T=T, H=H, k=8, E=32, seed=T + H + cluster, extra_rows=1)
+    inp = W.make_inputs(wl, "cuda")
+    want, y, s, _ = oracle_expert_norm(inp)
+    got, plan = run_expert_norm(inp, variant=mfr.VARIANT_CLUSTER, cluster_size=cluster)
+    assert plan.info()["cluster"] == cluster
+    assert_expert_norm_close(got, want, y, s)
+    assert plan.get_status() == 0
+
+
+def test_expert_norm_forms_reported():
+    """One CTA per token takes the one-pass form (rows held in registers) for
+    k <= 8 and at most two chunks per thread, unless its registers add a wave
+    of CTAs; else the two-pass form.  plan_info reports it as slot_registers."""
+    assert mfr.ExpertNormPlan(1, 4096, 8, variant=mfr.VARIANT_ROWS).info()["slot_registers"] == 1
+    assert mfr.ExpertNormPlan(1, 4096, 16, variant=mfr.VARIANT_ROWS).info()["slot_registers"] == 0
+    assert mfr.ExpertNormPlan(1, 16384, 8, variant=mfr.VARIANT_ROWS).info()["slot_registers"] == 0
+    assert mfr.ExpertNormPlan(1, 4096, 8).info()["slot_registers"] == 1      # the cluster form
 
 
 def test_expert_norm_stress_values_and_repeats():
@@ -89,7 +120,8 @@ def test_expert_norm_stress_values_and_repeats():
     assert np.array_equal(got, again)
 
 
-@pytest.mark.parametrize("variant", [mfr.VARIANT_ROWS, mfr.VARIANT_STREAM], ids=["rows", "ring"])
+@pytest.mark.parametrize("variant", [mfr.VARIANT_ROWS, mfr.VARIANT_STREAM, mfr.VARIANT_CLUSTER],
+                         ids=["rows", "ring", "cluster"])
 def test_expert_norm_bad_and_sentinel_slots(variant):
     inp = W.make_inputs(W.decode(8), "cuda")
     idx = inp["permuted_row_of"].clone()
@@ -131,7 +163,10 @@ def test_expert_norm_refuses_other_variants_and_other_plans():
     with pytest.raises(mfr.MFRError):
         mfr.ExpertNormPlan(64, 16384, 8, variant=mfr.VARIANT_STREAM)    # more than 4 column tiles
     with pytest.raises(mfr.MFRError):
-        mfr.ExpertNormPlan(64, 4096, 8, variant=mfr.VARIANT_CLUSTER)
+        mfr.ExpertNormPlan(64, 4096, 16, variant=mfr.VARIANT_CLUSTER)   # more than 8 slots
+    assert mfr.ExpertNormPlan(64, 4096, 8, variant=mfr.VARIANT_CLUSTER).info()["cluster"] > 1
+    assert mfr.ExpertNormPlan(1, 4096, 8).info()["variant"] == mfr.VARIANT_CLUSTER
+    assert mfr.ExpertNormPlan(1, 4096, 16).info()["variant"] == mfr.VARIANT_ROWS
     assert mfr.ExpertNormPlan(16384, 4096, 8).info()["variant"] == mfr.VARIANT_STREAM
     assert mfr.ExpertNormPlan(16384, 4096, 16).info()["variant"] == mfr.VARIANT_ROWS
     inp = W.make_inputs(W.decode(4), "cuda")

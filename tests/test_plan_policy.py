@@ -140,8 +140,11 @@ def test_per_expert_rmsnorm_rules(lib):
     assert rc == 0 and o["variant"] == mfr.VARIANT_STREAM
     rc, o, _ = choose(lib, 256, 4096, **ok)
     assert rc == 0 and (o["variant"], o["cluster"]) == (mfr.VARIANT_ROWS, 1)
-    rc, o, _ = choose(lib, 1, 4096, **ok)                                      # never a cluster
-    assert rc == 0 and (o["variant"], o["cluster"]) == (mfr.VARIANT_ROWS, 1)
+    for T, H, cluster in ((1, 4096, 4), (8, 4096, 16), (128, 4096, 2), (1, 8192, 8), (64, 8192, 4)):
+        rc, o, _ = choose(lib, T, H, **ok)                                   # the fused kernel's sizes
+        assert rc == 0 and (o["variant"], o["cluster"]) == (mfr.VARIANT_CLUSTER, cluster), (T, H)
+    rc, o, _ = choose(lib, 1, 4096, k=16, fused=False, en=True, stages=3)
+    assert rc == 0 and (o["variant"], o["cluster"]) == (mfr.VARIANT_ROWS, 1)  # more than 8 slots
     rc, o, _ = choose(lib, 16384, 4096, k=16, fused=False, en=True, stages=3)
     assert rc == 0 and o["variant"] == mfr.VARIANT_ROWS                      # more than 8 slots
     rc, _, _ = choose(lib, 16384, 4096, k=16, fused=False, en=True, stages=3, variant=mfr.VARIANT_STREAM)
@@ -154,5 +157,7 @@ def test_per_expert_rmsnorm_rules(lib):
     assert rc == 0 and o["variant"] == mfr.VARIANT_ROWS
     rc, _, _ = choose(lib, 16384, 8192, fused=False, en=True, stages=1, variant=mfr.VARIANT_STREAM)
     assert rc == ERR_SHAPE
-    rc, _, _ = choose(lib, 64, 4096, fused=False, en=True, stages=7, variant=mfr.VARIANT_CLUSTER)
-    assert rc == ERR_ARG
+    rc, o, _ = choose(lib, 64, 4096, fused=False, en=True, stages=7, variant=mfr.VARIANT_CLUSTER)
+    assert rc == 0 and o["variant"] == mfr.VARIANT_CLUSTER and o["cluster"] == 8
+    rc, _, _ = choose(lib, 64, 4096, k=9, fused=False, en=True, stages=7, variant=mfr.VARIANT_CLUSTER)
+    assert rc == ERR_SHAPE
