@@ -68,6 +68,26 @@ inline int decode_cluster(int chunks, int64_t elems) {
     return split(256);
 }
 
+// Cluster size for a small call of the per-expert RMSNorm form (measured on
+// GB300 as decode_cluster was, T = 1..128 at H = 4096 and 8192, two
+// repetitions within 0.5 %): up to 2^14 elements CTAs of 128 threads, up to
+// 2^16 CTAs of 64 threads (c16 at H = 8192, T = 4..8; c8 at H = 4096,
+// T = 16: 10 % faster than 16), up to 2^18 CTAs of 512 threads (one CTA per
+// token at H = 4096, two at 8192: 7-17 % faster than the fused kernel's
+// sizes), beyond that one CTA per token.  Its exchange carries 8 sums per
+// warp, so fewer, larger CTAs win earlier than in the fused kernel.
+inline int en_cluster(int chunks, int64_t elems) {
+    auto split = [chunks](int threads) {
+        int c = 1;
+        while (c < 16 && chunks / (2 * c) >= threads && chunks % (2 * c) == 0) c *= 2;
+        return c;
+    };
+    if (elems <= (int64_t(1) << 14)) return split(128);
+    if (elems <= (int64_t(1) << 16)) return split(64);
+    if (elems <= (int64_t(1) << 18)) return split(512);
+    return 1;
+}
+
 // Persistent CTAs for T tokens on `sms` SMs: the fewest rounds of one token
 // per CTA, over as few CTAs as give every CTA the same number of tokens (+-1).
 // T = 512 on 152 SMs: 128 CTAs x 4 tokens instead of 56 CTAs with 4 and 96
@@ -116,7 +136,7 @@ inline int choose_launch(const PolicyIn& in, PolicyOut* out, char* err, size_t e
         // ring kernel, which keeps a token's rows available until its slot
         // scales are known: k <= 8 and at most 4 column tiles (H <= 8192); two
         // tiles sit in registers and at most two stages are held, so two ring
-        // stages suffice.  The cluster sizes are those of the fused kernel.
+        // stages suffice.
         const bool ring_ok = in.k <= 8 && in.H <= 8192 && in.stages >= 2;
         const bool regs_ok = in.k <= 8;
         if (variant == MFR_VARIANT_CLUSTER && !regs_ok) {
@@ -130,7 +150,7 @@ inline int choose_launch(const PolicyIn& in, PolicyOut* out, char* err, size_t e
         if (variant == MFR_VARIANT_AUTO) {
             const int64_t elems = in.T * in.H;
             if (regs_ok && elems <= kClusterMaxElems) {
-                if (csize == 0) csize = decode_cluster(chunks, elems);
+                if (csize == 0) csize = en_cluster(chunks, elems);
                 variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
             } else {
                 variant = (ring_ok && elems >= kRowsMaxElems) ? MFR_VARIANT_STREAM : MFR_VARIANT_ROWS;
