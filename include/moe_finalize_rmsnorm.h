@@ -106,7 +106,9 @@ typedef struct mfr_plan_info {
     int sm_count;      /* SMs of the plan's device */
     int slot_registers; /* CLUSTER / ROWS: 1 = slot rows and weights held in registers
                            across the dependency wait, 0 = read from shared memory
-                           after it (chosen when the registers would cost a wave) */
+                           after it (chosen when the registers would cost a wave).
+                           Per-expert RMSNorm plans: 1 = the one-pass form (rows
+                           held in registers), 0 = the two-pass form */
 } mfr_plan_info;
 
 typedef struct mfr_plan_s* mfr_plan_t;
@@ -242,13 +244,15 @@ void moe_finalize_rmsnorm_destroy(mfr_plan_t plan);
  *     inv_j     = rsqrt(mean_h(E[r_j, :]^2) + eps)          (FP32, per row)
  *     out[t, h] = bf16( sum_j w[t,j] * ((E[r_j, h] * inv_j) * gamma[h]) )
  * with r_j = permuted_row_of[t, j], FP32 fused multiply-adds in slot order
- * j = 0..k-1, the shared gamma, and no residual.  Two kernels: one CTA per
- * token (MFR_VARIANT_ROWS), and for T*H >= 1.5*2^20 with k <= 8 and
- * H <= 8192 the persistent ring kernel (MFR_VARIANT_STREAM; forcing it
- * outside those limits is MFR_ERR_UNSUPPORTED_SHAPE); CLUSTER is refused.
+ * j = 0..k-1, the shared gamma, and no residual.  Variants: a cluster of
+ * CTAs per token that split H (MFR_VARIANT_CLUSTER, k <= 8; chosen for
+ * T*H <= 2^19), one CTA per token (MFR_VARIANT_ROWS), and for
+ * T*H >= 1.5*2^20 with k <= 8 and H <= 8192 the persistent ring kernel
+ * (MFR_VARIANT_STREAM).  Forcing CLUSTER with k > 8, or STREAM outside its
+ * limits, is MFR_ERR_UNSUPPORTED_SHAPE.
  *
  * moe_finalize_expert_rmsnorm_plan: as moe_finalize_rmsnorm_plan (same
- * shape rules and options; cluster_size is ignored).
+ * shape rules and options).
  * moe_finalize_expert_rmsnorm_run: expert_out bf16 [R, H], permuted_row_of
  * int32 [T, k], topk_weights fp32 [T, k], gamma bf16 [H], out bf16 [T, H];
  * device pointers, 16-byte aligned (4 for the index map and weights); out
