@@ -89,6 +89,20 @@ def test_automatic_choice(lib, T, H, variant, cluster):
         assert o["cpt"] * o["block"] >= chunks and o["block"] % 32 == 0 and o["block"] <= 512
 
 
+PLAIN_TABLE = [(1, 4096, 8), (2, 4096, 8), (4, 4096, 16), (8, 4096, 2), (16, 4096, 2), (32, 4096, 4),
+               (128, 4096, 4), (1, 8192, 16), (2, 8192, 16), (4, 8192, 4), (8, 8192, 4), (16, 8192, 8),
+               (64, 8192, 8)]
+
+
+@pytest.mark.parametrize("T,H,cluster", PLAIN_TABLE)
+def test_plain_finalize_split(lib, T, H, cluster):
+    """The plain finalize splits a token's columns over CTAs that share
+    nothing; its split sizes are its own."""
+    rc, o, _ = choose(lib, T, H, fused=False)
+    assert rc == 0 and (o["variant"], o["cluster"]) == (mfr.VARIANT_CLUSTER, cluster)
+    assert o["block"] * o["cpt"] * cluster >= H // 8
+
+
 def test_one_cta_geometry(lib):
     for H, cpt, block in ((24, 1, 32), (4096, 1, 512), (4104, 2, 288), (8192, 2, 512), (16384, 4, 512)):
         rc, o, _ = choose(lib, 300, H, variant=mfr.VARIANT_ROWS)
