@@ -146,6 +146,9 @@ def test_nvfp4_rules(lib):
     assert rc == 0 and o["variant"] == mfr.VARIANT_ROWS and o["cluster"] == 1
     rc, o, _ = choose(lib, 1, 4096, fp4=True)
     assert rc == 0 and o["cluster"] == 4
+    for T, H, cluster in ((8, 4096, 16), (32, 4096, 8), (16, 8192, 16), (64, 4096, 8)):
+        rc, o, _ = choose(lib, T, H, fp4=True)                               # 64-thread CTAs at 2^17
+        assert rc == 0 and o["cluster"] == cluster, (T, H, o)
 
 
 def test_per_expert_rmsnorm_rules(lib):
