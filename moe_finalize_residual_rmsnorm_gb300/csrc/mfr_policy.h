@@ -20,7 +20,8 @@ constexpr int kMaxStages = 8;           // ring kernel: deepest ring
 
 // Variant choice by the number of elements T*H of a call (measured on GB300
 // with cold inputs, CUDA graph): up to 2^19 a cluster of CTAs per token is
-// fastest (few tokens, latency bound; decode_cluster picks its size); below
+// fastest (few tokens, latency bound; decode_cluster, finalize_split and
+// en_cluster pick its size per plan kind); below
 // 1.5*2^20 one CTA per token; from there the persistent ring kernel (its
 // per-SM pipeline needs a few tokens per SM: at 1.5*2^20 it is 8 % faster at
 // H = 4096 and 3 % slower at H = 8192, at 2^21 faster at both, at 3*2^20 by

@@ -1,7 +1,7 @@
 // Persistent bulk-copy kernel (MFR_VARIANT_STREAM).
 //
 // At most one CTA per SM walks a static list of tokens (t = blockIdx.x,
-// += gridDim.x); the grid spreads the tokens evenly (stream_grid in mfr_api.cu).
+// += gridDim.x); the grid spreads the tokens evenly (stream_grid in mfr_policy.h).
 // A producer warp stages, for each token and each column tile of width
 // CB = 2048, the k gathered expert-row segments and the residual segment
 // into a ring of shared-memory stages with bulk asynchronous copies
