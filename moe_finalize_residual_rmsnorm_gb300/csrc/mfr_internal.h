@@ -47,6 +47,7 @@ struct Launch {
     int early_trigger;  // 1: signal dependents at kernel entry (small grids only)
     int regslots;     // one-CTA-per-token kernels: slot rows/weights held in registers
     int expert_norm;  // 1: RMSNorm per expert row before the weighted sum (mfr_expert_norm.cu)
+    int prefetch_out; // 1: the fused bf16 kernel also prefetches its output lines (smallest calls)
 };
 
 // Sets the calling thread's moe_finalize_rmsnorm_last_error() text.

@@ -49,8 +49,11 @@ namespace {
 // FUSED: residual + RMSNorm (true) or plain finalize (false); RS: each
 // thread holds the slot rows and weights in registers from before the
 // dependency wait (true), or reads them from shared memory as it loads (false:
-// 32 fewer registers, for CTAs whose residency the registers would halve).
-template <int CPT, int SG, bool FUSED, bool FP4, bool RS>
+// 32 fewer registers, for CTAs whose residency the registers would halve);
+// PFO: also ask L2 for the output lines before the wait (the smallest fused
+// bf16 calls, see kPrefetchOutMaxElems; a separate instantiation, so larger
+// calls keep the code they were tuned with).
+template <int CPT, int SG, bool FUSED, bool FP4, bool RS, bool PFO = false>
 __global__ void __launch_bounds__(kRowsMaxThreads)
 rows_kernel(const Params p, const int csize)
 {
@@ -117,6 +120,12 @@ rows_kernel(const Params p, const int csize)
                          static_cast<uint32_t>(nck) * 16u);
     else if (FUSED && tid == kMaxK)
         prefetch_l2_bulk(p.residual_in + t * p.H + col0, static_cast<uint32_t>(nck) * 32u);
+    if constexpr (PFO && FUSED && !FP4) {   // the output lines too
+        if (tid == kMaxK + 1)
+            prefetch_l2_bulk(p.residual_out + t * p.H + col0, static_cast<uint32_t>(nck) * 32u);
+        else if (tid == kMaxK + 2)
+            prefetch_l2_bulk(p.out + t * p.H + col0, static_cast<uint32_t>(nck) * 16u);
+    }
 
     // RS: slot rows and weights go to registers before the wait, so that
     // after it nothing but address arithmetic stands between the wait and the
@@ -317,7 +326,8 @@ RowsKernel pick_rows(bool fused, bool fp4) {
 // Shared-memory slot reads (RS = false) are instantiated only for one chunk
 // per thread: the only case where the registers cost residency (512-thread
 // CTAs at 64 vs 112 registers per thread).
-RowsKernel rows_kernel_for(int cpt, bool fused, bool fp4, bool regslots) {
+RowsKernel rows_kernel_for(int cpt, bool fused, bool fp4, bool regslots, bool pfo = false) {
+    if (pfo) return (cpt == 1 && fused && !fp4 && regslots) ? rows_kernel<1, 8, true, false, true, true> : nullptr;
     switch (cpt) {
         case 1: return regslots ? pick_rows<1, 8, true>(fused, fp4) : pick_rows<1, 8, false>(fused, fp4);
         case 2: return regslots ? pick_rows<2, 8, true>(fused, fp4) : nullptr;
@@ -385,7 +395,7 @@ cudaError_t rows_blocks_per_sm(const Launch& l, bool regslots, int* n) {
 }
 
 cudaError_t rows_prepare(const Launch& l) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0, l.prefetch_out != 0);
     if (!k) return cudaErrorInvalidValue;
     if (l.cluster > 8 && l.fused)
         return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -393,7 +403,7 @@ cudaError_t rows_prepare(const Launch& l) {
 }
 
 cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0, l.prefetch_out != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];
@@ -402,7 +412,7 @@ cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
 }
 
 cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0, l.prefetch_out != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];
