@@ -212,6 +212,14 @@ def recorded_traffic(workload: str, variant: str):
     return e.get("dram_bytes_per_launch")
 
 
+def workload_config(wl) -> dict:
+    """The workload keys of the JSON line's config, the same for both arms."""
+    return {"workload": f"{wl.name}: T={wl.T} H={wl.H} k={wl.k} E={wl.E} routing={wl.routing}"
+                        f"{'(s=%g)' % wl.zipf_s if wl.routing == 'zipf' else ''}",
+            "tokens_per_gpu": wl.T, "hidden": wl.H, "top_k": wl.k, "experts": wl.E,
+            "io": "bf16 expert rows and output, f32 residual in and out"}
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -352,10 +360,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "us_per_call": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp32 accumulate, bf16 out", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: T={T} H={H} k={k} E={wl.E} routing={wl.routing}"
-                               f"{'(s=%g)' % wl.zipf_s if wl.routing == 'zipf' else ''}",
-                   "tokens_per_gpu": T, "hidden": H, "top_k": k, "experts": wl.E,
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {**workload_config(wl),
                    "bytes_per_call": nbytes, "variant": info["variant_name"], "grid": info["grid_x"],
                    "block": info["block"], "cluster": info["cluster"], "pdl": not args.no_pdl,
                    "l2": f"inputs larger than L2 ({nbytes / 1e9:.2f} GB/call) and 2 alternating input sets",
@@ -661,8 +667,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp32 accumulate, bf16 out", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: T={wl.T} H={wl.H} k={wl.k} E={wl.E}", "tokens_per_gpu": wl.T},
+        "dtype": "f32", "data": "synthetic",
+        "config": {**workload_config(wl), "bytes_per_call": W.algorithmic_bytes(wl.T, wl.H, wl.k)},
         "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
