@@ -1,0 +1,47 @@
+"""bench.py's GPU arm prints the one JSON line the benchmark contract asks
+for, with the same workload config keys as the reference arm."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_bench(*args):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, out.stdout
+    return json.loads(lines[0])
+
+
+def test_gpu_arm_prints_the_contract_line():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    d = run_bench("--workload", "decode_T8", "--steps", "50", "--warmup", "3", "--cpu-seconds", "0.5")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
+                "clocks", "gpu_launches"):
+        assert key in d, key
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["n_gpus"] == 1 and d["dtype"] == "f32"
+    assert d["steps"] == 50 and d["warmup"] == 3 and d["value"] > 0 and d["gpu_launches"] == 50
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["single_thread"]["cores"] == 1
+    e = d["e2e"]
+    assert e["unit"] == "GB/s" and e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    ref = run_bench("--impl", "reference", "--workload", "decode_T8", "--steps", "3", "--warmup", "3",
+                    "--cpu-seconds", "0.05")
+    shared = {k: v for k, v in ref["config"].items() if k != "bytes_per_call"}
+    assert all(d["config"][k] == v for k, v in shared.items())
+    assert ref["config"]["bytes_per_call"] == d["config"]["bytes_per_call"]
+    assert ref["metric"] == d["metric"] and ref["unit"] == d["unit"] and ref["dtype"] == d["dtype"]
