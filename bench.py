@@ -220,6 +220,26 @@ def workload_config(wl) -> dict:
             "io": "bf16 expert rows and output, f32 residual in and out"}
 
 
+def host_cpu() -> str:
+    """The host CPU's name from /proc/cpuinfo (on Arm the implementer and part
+    numbers, which lscpu maps to names such as Neoverse-V2 for 0x41/0xd4f)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+    except OSError:
+        return os.uname().machine
+    fields = {}
+    for line in info:
+        if ":" in line:
+            key, _, val = line.partition(":")
+            fields.setdefault(key.strip().lower(), val.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "cpu part" in fields:
+        return f"{os.uname().machine} implementer {fields.get('cpu implementer', '?')} part {fields['cpu part']}"
+    return os.uname().machine
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -282,7 +302,7 @@ def cpu_baseline(inp_host, wl, target_s: float):
     # the same code on one thread, on a quarter of one thread's share of the sample
     dt1, n1 = time_oracle(inp_host, max(1, n // (4 * cores)), 1, 3)
     gbs1 = W.algorithmic_bytes(n1, wl.H, wl.k) / dt1 / 1e9
-    return {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "cpu": host_cpu(),
             "sample": f"{n} tokens drawn from the {wl.T}-token workload (seeded; whole shuffled passes "
                       f"when more than {wl.T}), H={wl.H}, k={wl.k}, {dt:.2f} s wall, {cores} host threads",
             "single_thread": {"value": round(gbs1, 4), "unit": UNIT, "cores": 1,
@@ -669,7 +689,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {**workload_config(wl), "bytes_per_call": W.algorithmic_bytes(wl.T, wl.H, wl.k)},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "cpu": host_cpu(),
+                         "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }), flush=True)
