@@ -54,6 +54,19 @@ def test_finalize_only_matches_oracle(kw, T, H, k):
     assert plan.get_status() == 0
 
 
+@pytest.mark.parametrize("T,H", [(1, 4096), (4, 4096), (2, 8192), (33, 8192)])
+@pytest.mark.parametrize("split", [2, 4, 8, 16])
+def test_finalize_only_every_split(T, H, split):
+    """Every number of CTAs per token, against the oracle, bitwise."""
+    wl = W.Workload(f"fin_s{split}_T{T}_H{H}", T=T, H=H, k=8, E=32, seed=T + H + split, extra_rows=1)
+    inp = W.make_inputs(wl, "cuda")
+    want, _ = oracle_finalize_only(inp)
+    got, plan = run_finalize(inp, variant=mfr.VARIANT_CLUSTER, cluster_size=split)
+    assert plan.info()["cluster"] == split
+    assert np.array_equal(got, want)
+    assert plan.get_status() == 0
+
+
 def test_finalize_only_bad_indices():
     inp = W.make_inputs(W.decode(8), "cuda")
     inp["permuted_row_of"][2, 5] = -1

@@ -104,6 +104,9 @@ CASES = [
     ("stress_T40", W.STRESS.with_(T=40), {}),
     ("H16384_T5", W.Workload("h16k", T=5, H=16384, k=8, E=32), {}),
     ("H1040_T7_cluster", W.Workload("h1040", T=7, H=1040, k=5, E=16), dict(variant=mfr.VARIANT_CLUSTER)),
+    ("decode_T32_cluster8", W.decode(32), {}),                           # 64-thread CTAs at 2^17
+    ("decode_T4_cluster16", W.decode(4), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=16)),
+    ("wide_T2_cluster16", W.wide(2), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=16)),
 ]
 
 
