@@ -228,6 +228,16 @@ int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_s
  * floor of a call.  Touches no memory.  T == 0 is a no-op. */
 int moe_finalize_rmsnorm_launch_floor(mfr_plan_t plan, void* stream);
 
+/* Failure-path self test.  Enqueues one thread that waits on an on-chip
+ * barrier with the same bounded-wait routine every kernel of the library uses
+ * (each of their waits gives up after about 2 s and sets MFR_STATUS_TIMEOUT),
+ * but with a limit of `limit_cycles` SM clock cycles; the barrier receives its
+ * arrival only if `arrive` is nonzero.  When the wait runs out the kernel sets
+ * MFR_STATUS_TIMEOUT in the plan's status word and returns, so the context
+ * stays usable; read it with _get_status.  limit_cycles must be in
+ * [1, 2^32], else MFR_ERR_INVALID_ARG. */
+int moe_finalize_rmsnorm_wait_selftest(mfr_plan_t plan, int64_t limit_cycles, int arrive, void* stream);
+
 /* Copies what the plan decided into *info. */
 int moe_finalize_rmsnorm_plan_info(mfr_plan_t plan, mfr_plan_info* info);
 

@@ -70,6 +70,7 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_get_status": (_I, [_VP, _VP, ctypes.POINTER(_I)]),
     "moe_finalize_rmsnorm_plan_info": (_I, [_VP, ctypes.POINTER(PlanInfo)]),
     "moe_finalize_rmsnorm_launch_floor": (_I, [_VP, _VP]),
+    "moe_finalize_rmsnorm_wait_selftest": (_I, [_VP, ctypes.c_int64, ctypes.c_int, _VP]),
     "moe_finalize_rmsnorm_bench_producer": (_I, [_VP, _VP, _I64, _I64, ctypes.c_longlong, _I, _VP]),
     "moe_finalize_rmsnorm_host_workspace_bytes": (_I64, [_VP]),
     "moe_finalize_rmsnorm_run_host": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _VP, _I64, _VP]),
@@ -208,6 +209,14 @@ class Plan:
         return self._lib.moe_finalize_rmsnorm_run(self._h, expert_out, permuted_row_of, topk_weights,
                                                   residual_in, residual_out, gamma, ctypes.c_float(eps),
                                                   out, stream)
+
+    def wait_selftest(self, limit_cycles: int, arrive: bool, stream=None) -> None:
+        """One bounded on-chip wait that runs out unless `arrive`; a wait that
+        runs out sets STATUS_TIMEOUT in the plan's status word
+        (C: moe_finalize_rmsnorm_wait_selftest)."""
+        _check(self._lib.moe_finalize_rmsnorm_wait_selftest(self._h, int(limit_cycles), int(bool(arrive)),
+                                                            _stream_handle(stream)),
+               "moe_finalize_rmsnorm_wait_selftest")
 
     def launch_floor(self, stream=None) -> None:
         """Enqueues the empty kernel with this plan's launch geometry."""

@@ -613,6 +613,20 @@ int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_s
     return MFR_OK;
 }
 
+int moe_finalize_rmsnorm_wait_selftest(mfr_plan_t plan, int64_t limit_cycles, int arrive, void* stream) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    if (limit_cycles < 1 || limit_cycles > (int64_t(1) << 32))
+        return fail(MFR_ERR_INVALID_ARG, "limit_cycles must be in [1, 2^32] (got %lld)", (long long)limit_cycles);
+    const cudaError_t e = mfr::wait_selftest_launch(plan->d_status, static_cast<long long>(limit_cycles),
+                                                    arrive ? 1 : 0, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_LAUNCH, "self-test kernel launch", e);
+    }
+    return MFR_OK;
+}
+
 int moe_finalize_rmsnorm_launch_floor(mfr_plan_t plan, void* stream) {
     g_last_error[0] = '\0';
     if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");

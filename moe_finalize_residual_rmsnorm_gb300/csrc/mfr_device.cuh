@@ -93,14 +93,20 @@ __device__ __forceinline__ bool mbar_test_parity(uint32_t bar, uint32_t parity) 
     return done != 0;
 }
 
-// Waits (bounded, ~2 s at 2 GHz) for the phase with this parity to complete.
-constexpr long long kWaitCycles = 4000000000LL;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Waits at most `limit` SM cycles for the phase with this parity to
+// complete; false if it did not.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit) {
     if (mbar_test_parity(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_test_parity(bar, parity))
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     return true;
+}
+
+// Every wait of the kernels: bounded at ~2 s at 2 GHz.
+constexpr long long kWaitCycles = 4000000000LL;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    return mbar_wait_bounded(bar, parity, kWaitCycles);
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.

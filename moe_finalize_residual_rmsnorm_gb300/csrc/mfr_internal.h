@@ -62,6 +62,8 @@ cudaError_t rows_max_active_clusters(const Launch& l, int* n);
 cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s);
 // An empty kernel with the plan's launch geometry (for the launch floor).
 cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s);
+// One bounded wait that runs out unless `arrive` (tests of the failure path).
+cudaError_t wait_selftest_launch(int* status, long long limit, int arrive, cudaStream_t s);
 
 // mfr_expert_norm.cu: each expert row RMS-normalised before the weighted
 // sum.  With regslots the one-pass kernel (k <= 8, cpt <= 2; a cluster of

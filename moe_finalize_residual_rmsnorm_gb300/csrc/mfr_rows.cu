@@ -368,7 +368,25 @@ __global__ void floor_kernel(int* status) {
     if (status == nullptr && threadIdx.x == 0x7FFFFFFF) *status = 0;  // never taken; keeps the argument
 }
 
+// One thread waits, with the kernels' bounded-wait helper, on an mbarrier
+// that gets its one arrival only if `arrive`; a wait that runs out sets
+// MFR_STATUS_TIMEOUT.  Exercises the failure path without faulting anything.
+__global__ void wait_selftest_kernel(int* status, long long limit, int arrive) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_addr(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (arrive) mbar_arrive(smem_addr(&bar));
+    if (!mbar_wait_bounded(smem_addr(&bar), 0, limit))
+        atomicOr(status, MFR_STATUS_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t wait_selftest_launch(int* status, long long limit, int arrive, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit, arrive);
+    return cudaGetLastError();
+}
 
 cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s) {
     if (l.smem_bytes > 0) {
