@@ -12,6 +12,7 @@ built, importing the binding's entry points raises.
 """
 from __future__ import annotations
 
+import collections
 import ctypes
 import os
 from typing import Optional
@@ -373,11 +374,39 @@ def run_noalloc(expert_out, permuted_row_of, topk_weights, residual_in, residual
     return st.value if report_status else None
 
 
+PLAN_CACHE_SIZE = 64
+_plan_cache: "collections.OrderedDict" = collections.OrderedDict()
+
+
+def cached_plan(T: int, H: int, k: int, R: int, **plan_kw) -> Plan:
+    """The plan for (current device, T, H, k, R, options), made once and kept
+    in a per-process cache of the PLAN_CACHE_SIZE most recently used plans.
+    Plans are immutable, so one may serve calls on several streams.  A plan
+    holds one device status word: an evicted plan is destroyed after its
+    device has finished all queued work.  Make the plan before a CUDA graph
+    capture, and keep plans that a graph uses outside the cache (Plan(...)),
+    since a graph must not outlive its plans."""
+    import torch
+    key = (torch.cuda.current_device(), int(T), int(H), int(k), int(R), tuple(sorted(plan_kw.items())))
+    plan = _plan_cache.get(key)
+    if plan is None:
+        plan = Plan(T, H, k, R, **plan_kw)
+        _plan_cache[key] = plan
+        while len(_plan_cache) > PLAN_CACHE_SIZE:
+            (dev, *_), old = _plan_cache.popitem(last=False)
+            torch.cuda.synchronize(dev)     # no run of the old plan is still in flight
+            old.close()
+    else:
+        _plan_cache.move_to_end(key)
+    return plan
+
+
 def moe_finalize_residual_rmsnorm(expert_out, permuted_row_of, topk_weights, residual, gamma, eps: float,
                                   *, residual_out=None, out=None, stream=None, plan: Optional[Plan] = None,
                                   **plan_kw):
     """Allocating convenience wrapper: returns (residual_out, out).  With
-    residual_out=residual the update is in place."""
+    residual_out=residual the update is in place.  Without `plan` it takes
+    the cached plan for the shapes and options (cached_plan)."""
     import torch
     T, k = permuted_row_of.shape
     R, H = expert_out.shape
@@ -386,7 +415,7 @@ def moe_finalize_residual_rmsnorm(expert_out, permuted_row_of, topk_weights, res
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=residual.device)
     if plan is None:
-        plan = Plan(T, H, k, R, **plan_kw)
+        plan = cached_plan(T, H, k, R, **plan_kw)
     plan.run(expert_out, permuted_row_of, topk_weights, residual, residual_out, gamma, eps, out, stream)
     return residual_out, out
 

@@ -370,3 +370,33 @@ def test_sentinel_skip_for_non_local_experts(kw):
     idx[2, 2] = R                                         # out of range at the top: always an error
     got_res, got_out, plan = run_gpu(inp, dict(kw, sentinel_skip=True))
     assert plan.get_status() & mfr.STATUS_BAD_INDEX
+
+
+def test_functional_wrapper_caches_plans():
+    """The allocating wrapper reuses one plan per shape and options and keeps
+    at most PLAN_CACHE_SIZE of them."""
+    inp = W.make_inputs(W.decode(2), "cuda")
+    want_res, want_out, _ = oracle_on(inp)
+    args = (inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], inp["residual"], inp["gamma"],
+            inp["eps"])
+    mfr._plan_cache.clear()
+    for _ in range(3):
+        res, out = mfr.moe_finalize_residual_rmsnorm(*args)
+        torch.cuda.synchronize()
+        assert_residual_close(f32(res), want_res)
+        assert_out_close(bf16_bits(out), want_out)
+    assert len(mfr._plan_cache) == 1
+    mfr.moe_finalize_residual_rmsnorm(*args, variant=mfr.VARIANT_ROWS)
+    assert len(mfr._plan_cache) == 2
+    old = mfr.PLAN_CACHE_SIZE
+    try:
+        mfr.PLAN_CACHE_SIZE = 2
+        for T in (1, 3, 5):
+            x = W.make_inputs(W.decode(T), "cuda")
+            mfr.moe_finalize_residual_rmsnorm(x["expert_out"], x["permuted_row_of"], x["topk_weights"],
+                                              x["residual"], x["gamma"], x["eps"])
+        torch.cuda.synchronize()
+        assert len(mfr._plan_cache) == 2
+    finally:
+        mfr.PLAN_CACHE_SIZE = old
+        mfr._plan_cache.clear()
