@@ -460,7 +460,9 @@ def run_sweep(mfr, device, args):
                    steady state.
       loop_us      the same calls launched one by one from Python through the C
                    ABI (pointers taken once), CUDA events around 200+ calls,
-                   median of 5 batches (host-bound for small calls: context only).
+                   median of 5 batches; loop_vs_2x_floor is the decode target
+                   on this loop and its floor (host-bound for small calls, so
+                   it says little about the kernel: the graph figure does).
       warm_us      the graph over a single input set (inputs in L2; context only).
     The floor is the same graph (or loop) of empty kernels with the identical
     launch geometry and PDL attribute (moe_finalize_rmsnorm_launch_floor);
@@ -550,7 +552,8 @@ def run_sweep(mfr, device, args):
                      "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1), "floor_us": round(floor_us, 3),
                      "vs_2x_floor": round(us / target, 3), "variant": info["variant_name"],
                      "cluster": info["cluster"], "sets": nsets, "graph_calls": ncalls,
-                     "warm_us": round(warm, 3), "loop_us": round(loop, 3), "loop_floor_us": round(loop_floor, 3)})
+                     "warm_us": round(warm, 3), "loop_us": round(loop, 3), "loop_floor_us": round(loop_floor, 3),
+                     "loop_vs_2x_floor": round(loop / (2 * (loop_floor + nbytes / 8e12 * 1e6)), 3)})
         if plan.get_status(stream) != 0:
             raise RuntimeError(f"the device status word reported an error during {wl.name}")
         del E, idx, w, res, rout, out, base
