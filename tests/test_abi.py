@@ -111,3 +111,38 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
         mfr.load_library()
     with pytest.raises(ImportError):
         mfr.Plan(1, 4096, 8)
+
+
+def test_header_compiles_as_c_and_links_from_a_c_program(lib, tmp_path):
+    """The boundary is plain C: a C99 program that includes only the header
+    compiles with gcc, links against the library and gets the host-side
+    answers (no GPU here: a plan reports MFR_ERR_BAD_DEVICE)."""
+    import importlib
+    import subprocess
+    libpath = importlib.import_module("moe_finalize_residual_rmsnorm_gb300.build").LIBRARY
+    src = tmp_path / "use_abi.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe_finalize_rmsnorm.h"
+int main(void) {
+    mfr_options o;
+    mfr_plan_t plan = NULL;
+    moe_finalize_rmsnorm_default_options(&o);
+    if (moe_finalize_rmsnorm_supports(4096, 8) != 1 || moe_finalize_rmsnorm_supports(4100, 8) != 0) return 1;
+    if (strcmp(moe_finalize_rmsnorm_strerror(MFR_OK), "ok") != 0) return 2;
+    int rc = moe_finalize_rmsnorm_plan(&plan, 8, 4096, 8, 64, &o);
+    if (rc != MFR_OK && plan != NULL) return 3;
+    printf("%d\n", rc);
+    if (plan) moe_finalize_rmsnorm_destroy(plan);
+    return 0;
+}
+""")
+    exe = tmp_path / "use_abi"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", f"-I{HEADER_DIR}", str(src), "-o", str(exe),
+                    libpath, f"-Wl,-rpath,{os.path.dirname(libpath)}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out
+    rc = int(out.stdout.strip())
+    expected = mfr.MFR_OK if torch.cuda.is_available() else 4    # MFR_ERR_BAD_DEVICE
+    assert rc == expected
