@@ -95,14 +95,16 @@ inline int finalize_split(int chunks, int64_t elems) {
 
 // Cluster size for a small call of the per-expert RMSNorm form (measured on
 // GB300 as decode_cluster was, T = 1..128 at H = 4096 and 8192, two
-// repetitions within 0.5 %): up to 2^14 elements CTAs of 128 threads, up to
-// 2^16 CTAs of 64 threads (c16 at H = 8192, T = 4..8; c8 at H = 4096,
-// T = 16: 10 % faster than 16), up to 2^18 CTAs of 512 threads (one CTA per
-// token at H = 4096, two at 8192: 7-17 % faster than the fused kernel's
-// sizes), beyond that one CTA per token.  Its exchange carries 8 sums per
-// warp, so fewer, larger CTAs win earlier than in the fused kernel.
+// repetitions within 0.5 %): up to 2^13 elements CTAs of 128 threads, up to
+// 2^15 CTAs of 32 (16 CTAs per token: T = 4 at H = 4096 1.88 us against 2.02
+// with 128-thread CTAs), up to 2^16 CTAs of 64 (c16 at H = 8192, T = 8; c8
+// at H = 4096, T = 16: 10 % faster than 16), up to 2^18 CTAs of 512 threads
+// (one CTA per token at H = 4096, two at 8192: 7-17 % faster than the fused
+// kernel's sizes), beyond that one CTA per token.  Its exchange carries 8
+// sums per warp, so fewer, larger CTAs win earlier than in the fused kernel.
 inline int en_cluster(int chunks, int64_t elems) {
-    if (elems <= (int64_t(1) << 14)) return split_for_threads(chunks, 128);
+    if (elems <= (int64_t(1) << 13)) return split_for_threads(chunks, 128);
+    if (elems <= (int64_t(1) << 15)) return split_for_threads(chunks, 32);
     if (elems <= (int64_t(1) << 16)) return split_for_threads(chunks, 64);
     if (elems <= (int64_t(1) << 18)) return split_for_threads(chunks, 512);
     return 1;

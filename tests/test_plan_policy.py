@@ -157,9 +157,9 @@ def test_per_expert_rmsnorm_rules(lib):
     assert rc == 0 and o["variant"] == mfr.VARIANT_STREAM
     rc, o, _ = choose(lib, 256, 4096, **ok)
     assert rc == 0 and (o["variant"], o["cluster"]) == (mfr.VARIANT_ROWS, 1)
-    for T, H, cluster in ((1, 4096, 4), (4, 4096, 4), (8, 4096, 8), (16, 4096, 8), (32, 4096, 1),
-                          (128, 4096, 1), (1, 8192, 8), (2, 8192, 8), (4, 8192, 16), (8, 8192, 16),
-                          (16, 8192, 2), (32, 8192, 2), (64, 8192, 1)):
+    for T, H, cluster in ((1, 4096, 4), (2, 4096, 4), (4, 4096, 16), (8, 4096, 16), (16, 4096, 8),
+                          (32, 4096, 1), (128, 4096, 1), (1, 8192, 8), (2, 8192, 16), (4, 8192, 16),
+                          (8, 8192, 16), (16, 8192, 2), (32, 8192, 2), (64, 8192, 1)):
         rc, o, _ = choose(lib, T, H, **ok)
         want = mfr.VARIANT_CLUSTER if cluster > 1 else mfr.VARIANT_ROWS
         assert rc == 0 and (o["variant"], o["cluster"]) == (want, cluster), (T, H, o)
