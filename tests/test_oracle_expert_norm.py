@@ -135,3 +135,26 @@ def test_output_is_the_nearest_bf16_and_tokens_select_rows(oracle_lib):
     sub = [5, 0, 3]
     part, _ = oracle_lib.finalize_expert_rmsnorm(E, idx, w, gamma, 1e-6, tokens=sub)
     assert np.array_equal(part, out[sub])
+
+
+def test_hand_worked_example(oracle_lib):
+    """tests/golden/expert_rmsnorm_hand_worked.json: two tokens worked by hand
+    (powers of two throughout, so every value is exact and so are the BF16
+    results)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "expert_rmsnorm_hand_worked.json")
+    g = json.load(open(path))
+    E = np.array([[int(b, 16) for b in row] for row in g["expert_out_bits"]], dtype=np.uint16)
+    gamma = np.array([int(b, 16) for b in g["gamma_bits"]], dtype=np.uint16)
+    np.testing.assert_array_equal(bf16_bits_to_f64(E), np.array(g["expert_out"], dtype=np.float64))
+    np.testing.assert_array_equal(bf16_bits_to_f64(gamma), np.array(g["gamma"], dtype=np.float64))
+    idx = np.array(g["permuted_row_of"], dtype=np.int32)
+    w = np.array(g["topk_weights"], dtype=np.float32)
+    y, bad = oracle_lib.expert_rmsnorm_f64(E, idx, w, gamma, g["eps"])
+    assert bad == 0
+    np.testing.assert_array_equal(y, np.array(g["expected_out"], dtype=np.float64))
+    out, bad = oracle_lib.finalize_expert_rmsnorm(E, idx, w, gamma, g["eps"])
+    assert bad == 0
+    want = np.array([[int(b, 16) for b in row] for row in g["expected_out_bits"]], dtype=np.uint16)
+    np.testing.assert_array_equal(out, want)
