@@ -30,8 +30,8 @@
 //   sum      : acc = fma(c_j, e_j, acc) in slot order from the registers
 //   store    : bf16(gamma * acc)
 // expert_norm_kernel (any k <= 16, up to four chunks per thread): one CTA per
-// token in two passes; pass 1 forms the per-slot sums of squares as above
-// (warps summed in index order), pass 2 reloads the rows (L2 hits, read
+// token in two passes; pass 1 forms the per-slot sums of squares (per slot a
+// warp butterfly, then the warps in index order), pass 2 reloads the rows (L2 hits, read
 // microseconds earlier) for the weighted sum, so no thread holds k rows.
 // The ring kernel (mfr_stream.cu, EN) computes the same for large calls with
 // k <= 8 and H <= 8192.  HBM sees every row once in all three.  Every order
