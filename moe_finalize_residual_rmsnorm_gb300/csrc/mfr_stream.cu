@@ -192,7 +192,8 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                                 bulk_g2s(smem_u32(st + kHeaderBytes + j * row_bytes),
                                          p.expert_out + static_cast<int64_t>(rl[j]) * H + c0,
                                          static_cast<uint32_t>(cb * 2), bar);
-                        bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
+                        if (FUSED)   // only fused stages carry a residual segment (and count its bytes)
+                            bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
                     }
                 }
                 ++fill;
