@@ -9,6 +9,7 @@ import ctypes
 import os
 import subprocess
 
+import numpy as np
 import pytest
 
 import moe_finalize_residual_rmsnorm_gb300 as mfr
@@ -181,3 +182,54 @@ def test_per_expert_rmsnorm_rules(lib):
     assert rc == 0 and o["variant"] == mfr.VARIANT_CLUSTER and o["cluster"] == 8
     rc, _, _ = choose(lib, 64, 4096, k=9, fused=False, en=True, stages=7, variant=mfr.VARIANT_CLUSTER)
     assert rc == ERR_SHAPE
+
+
+def test_every_choice_fits_its_kernel(lib):
+    """Over many shapes, plan kinds and options, whatever the policy returns
+    is a geometry its kernel can run: whole warps, at most 512 threads, every
+    16-byte chunk owned by one thread, a cluster that splits the chunks
+    evenly (NVFP4: whole 16-column blocks per CTA), the per-expert cluster
+    and one-pass forms within 8 slots, the ring within its slot and tile
+    limits, and the persistent grid no larger than the SM count."""
+    rng = np.random.default_rng(123)
+    variants = (mfr.VARIANT_AUTO, mfr.VARIANT_CLUSTER, mfr.VARIANT_ROWS, mfr.VARIANT_STREAM)
+    checked = 0
+    for _ in range(20000):
+        H = int(rng.integers(1, 2049)) * 8
+        T = int(rng.choice([1, 2, 3, 5, 8, 16, 33, 64, 100, 128, 200, 512, 1000, 4096, 20000]))
+        k = int(rng.integers(1, 17))
+        kind = int(rng.integers(0, 4))          # 0 fused, 1 plain, 2 NVFP4, 3 per-expert
+        fused, fp4, en = kind in (0, 2), kind == 2, kind == 3
+        if fp4 and H % 16:
+            continue
+        variant = int(rng.choice(variants))
+        cluster = int(rng.choice([0, 0, 1, 2, 4, 8, 16]))
+        stages = int(rng.integers(0, 9))
+        rc, o, err = choose(lib, T, H, k=k, fused=fused, fp4=fp4, en=en, variant=variant, cluster=cluster,
+                            stages=stages)
+        if rc != mfr.MFR_OK:
+            assert rc in (ERR_ARG, ERR_SHAPE) and err, (T, H, k, kind, variant, cluster, stages)
+            continue
+        checked += 1
+        chunks = H // 8
+        assert o["variant"] in (mfr.VARIANT_CLUSTER, mfr.VARIANT_ROWS, mfr.VARIANT_STREAM)
+        if variant != mfr.VARIANT_AUTO:
+            assert o["variant"] == variant or (variant == mfr.VARIANT_CLUSTER and o["variant"] == mfr.VARIANT_ROWS)
+        if o["variant"] == mfr.VARIANT_STREAM:
+            assert stages >= 2 and o["block"] == RING_THREADS and 1 <= o["grid_x"] <= min(T, SMS)
+            assert -(-H // 2048) <= 8
+            if en:
+                assert k <= 8 and H <= 8192
+            continue
+        c = o["cluster"]
+        assert c in (1, 2, 4, 8, 16) and chunks % c == 0
+        assert (c > 1) == (o["variant"] == mfr.VARIANT_CLUSTER)
+        per_cta = chunks // c
+        assert o["cpt"] in (1, 2, 4) and o["block"] % 32 == 0 and 32 <= o["block"] <= 512
+        assert o["block"] * o["cpt"] >= per_cta and (o["block"] - 32) * o["cpt"] < per_cta
+        assert o["grid_x"] == T * c
+        if fp4 and c > 1:
+            assert per_cta % 2 == 0
+        if en and c > 1:
+            assert k <= 8 and o["cpt"] <= 2
+    assert checked > 5000
