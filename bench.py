@@ -464,6 +464,8 @@ def run_sweep(mfr, device, args):
                    on this loop and its floor (host-bound for small calls, so
                    it says little about the kernel: the graph figure does).
       warm_us      the graph over a single input set (inputs in L2; context only).
+      other_outputs_us  at T <= 8, the plain finalize, NVFP4 and per-expert
+                   RMSNorm outputs timed like us_per_call.
     The floor is the same graph (or loop) of empty kernels with the identical
     launch geometry and PDL attribute (moe_finalize_rmsnorm_launch_floor);
     the decode target is us_per_call <= 2 * (floor_us + bytes / 8 TB/s)."""
@@ -546,6 +548,42 @@ def run_sweep(mfr, device, args):
             warm = graph_us(False, 1)
             loop = loop_us(False)
             loop_floor = loop_us(True)
+            # the other outputs at decode sizes, timed the same way (graph, cold sets)
+            others = {}
+            if T <= 8:
+                q = torch.empty((nsets, T, H // 2), dtype=torch.uint8, device=device)
+                sf = torch.empty((nsets, T, H // 16), dtype=torch.uint8, device=device)
+                kinds = {
+                    "finalize_only": (mfr.FinalizePlan(T, H, k, R, enable_pdl=not args.no_pdl),
+                                      lambda pl, j: pl.run(E[j], idx[j], w[j], out[j], stream, validate=False)),
+                    "nvfp4_epilogue": (mfr.Nvfp4Plan(T, H, k, R, enable_pdl=not args.no_pdl),
+                                       lambda pl, j: pl.run(E[j], idx[j], w[j], res[j], rout[j], g, base["eps"],
+                                                            448.0 * 6.0 / 16.0, q[j], sf[j], stream,
+                                                            validate=False)),
+                    "expert_rmsnorm": (mfr.ExpertNormPlan(T, H, k, R, enable_pdl=not args.no_pdl),
+                                       lambda pl, j: pl.run(E[j], idx[j], w[j], g, base["eps"], out[j], stream,
+                                                            validate=False)),
+                }
+                for name, (pl, call) in kinds.items():
+                    graph = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(graph, stream=stream):
+                        for i in range(ncalls):
+                            call(pl, i % nsets)
+                    graph.replay()
+                    stream.synchronize()
+                    times = []
+                    for _ in range(5):
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        graph.replay()
+                        b.record(stream)
+                        b.synchronize()
+                        times.append(a.elapsed_time(b) * 1e3 / ncalls)
+                    del graph
+                    if pl.get_status(stream) != 0:
+                        raise RuntimeError(f"the device status word reported an error during {wl.name} {name}")
+                    others[name] = round(float(np.median(times)), 3)
+                del q, sf
         info = plan.info()
         target = 2 * (floor_us + nbytes / 8e12 * 1e6)
         rows.append({"workload": wl.name, "T": T, "H": H, "us_per_call": round(us, 3),
@@ -553,7 +591,8 @@ def run_sweep(mfr, device, args):
                      "vs_2x_floor": round(us / target, 3), "variant": info["variant_name"],
                      "cluster": info["cluster"], "sets": nsets, "graph_calls": ncalls,
                      "warm_us": round(warm, 3), "loop_us": round(loop, 3), "loop_floor_us": round(loop_floor, 3),
-                     "loop_vs_2x_floor": round(loop / (2 * (loop_floor + nbytes / 8e12 * 1e6)), 3)})
+                     "loop_vs_2x_floor": round(loop / (2 * (loop_floor + nbytes / 8e12 * 1e6)), 3),
+                     **({"other_outputs_us": others} if others else {})})
         if plan.get_status(stream) != 0:
             raise RuntimeError(f"the device status word reported an error during {wl.name}")
         del E, idx, w, res, rout, out, base
