@@ -33,6 +33,10 @@ def draw_cases(n=48, seed=2026):
     return cases
 
 
+def pdl_of(seed):
+    return seed % 3 != 0          # a third of the cases launch without programmatic dependent launch
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _library():
     if not torch.cuda.is_available():
@@ -47,7 +51,7 @@ def test_random_shape_matches_oracle(kind, T, H, k, variant, cluster, seed):
     wl = W.Workload(f"fuzz_{kind}_T{T}_H{H}_k{k}", T=T, H=H, k=k, E=max(16, 2 * k), seed=seed % 100000,
                     extra_rows=int(seed % 5))
     inp = W.make_inputs(wl, "cuda")
-    kw = dict(variant=variant)
+    kw = dict(variant=variant, enable_pdl=pdl_of(seed))
     if cluster:
         kw["cluster_size"] = cluster
     try:
