@@ -400,3 +400,33 @@ def test_functional_wrapper_caches_plans():
     finally:
         mfr.PLAN_CACHE_SIZE = old
         mfr._plan_cache.clear()
+
+
+@pytest.mark.parametrize("kw", [dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_STREAM),
+                                dict(variant=mfr.VARIANT_CLUSTER, cluster_size=4)],
+                         ids=["rows", "stream", "cluster4"])
+def test_every_slot_non_local(kw):
+    """A batch whose experts all live on other GPUs: R = 0 and every index -1
+    with sentinel_skip.  No row is read, the residual passes through
+    unchanged, out is the RMSNorm of the residual alone, the plain finalize
+    and the per-expert form write zeros, and no status bit is raised."""
+    T, H, k = 6, 4096, 8
+    inp = W.make_inputs(W.decode(T), "cuda")
+    inp["expert_out"] = torch.empty((0, H), dtype=torch.bfloat16, device="cuda")
+    inp["permuted_row_of"] = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+    plan = mfr.Plan(T, H, k, 0, sentinel_skip=True, **kw)
+    got_res, got_out, _ = run_gpu(inp, plan=plan)
+    assert np.array_equal(got_res.view(np.uint32), f32(inp["residual"]).view(np.uint32))
+    want_res, want_out, _ = oracle_on(inp)
+    assert_out_close(got_out, want_out)
+    assert plan.get_status() == 0
+    for make in (mfr.FinalizePlan, mfr.ExpertNormPlan):
+        p = make(T, H, k, 0, sentinel_skip=True, **kw)
+        out = torch.full((T, H), 7.0, dtype=torch.bfloat16, device="cuda")
+        if make is mfr.FinalizePlan:
+            p.run(inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], out)
+        else:
+            p.run(inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], inp["gamma"], inp["eps"], out)
+        torch.cuda.synchronize()
+        assert torch.all(out.float() == 0)
+        assert p.get_status() == 0
