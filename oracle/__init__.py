@@ -96,6 +96,8 @@ class Oracle:
         lib.mfr_oracle_e2m1_to_f64.restype = ctypes.c_double
         lib.mfr_oracle_nvfp4_quantize.argtypes = [i64, i64, p, ctypes.c_float, p, p]
         lib.mfr_oracle_nvfp4_quantize.restype = None
+        lib.mfr_oracle_nvfp4_encode.argtypes = [i64, i64, p, ctypes.c_float, p, p]
+        lib.mfr_oracle_nvfp4_encode.restype = None
         lib.mfr_oracle_finalize_residual_rmsnorm_nvfp4.argtypes = [
             i64, i64, i64, i64, p, p, p, p, p, ctypes.c_float, ctypes.c_float, p, p, p, p, i64, p, p]
         lib.mfr_oracle_finalize_residual_rmsnorm_nvfp4.restype = i64
@@ -262,6 +264,18 @@ class Oracle:
         self.lib.mfr_oracle_nvfp4_quantize(n, H, _ptr(y), ctypes.c_float(s_enc), _ptr(q), _ptr(sf))
         return q, sf
 
+    def nvfp4_encode(self, y, s_enc: float, sf):
+        """The codes of y float32 [n, H] for block scales chosen by the caller
+        (sf uint8 [n, H/16]), by the quantiser's steps after its scale
+        choice.  Returns packed codes uint8 [n, H/2]."""
+        y = _c(y, np.float32)
+        sf = _c(sf, np.uint8)
+        n, H = y.shape
+        assert H % 16 == 0 and sf.shape == (n, H // 16)
+        q = np.empty((n, H // 2), dtype=np.uint8)
+        self.lib.mfr_oracle_nvfp4_encode(n, H, _ptr(y), ctypes.c_float(s_enc), _ptr(sf), _ptr(q))
+        return q
+
     def finalize_residual_rmsnorm_nvfp4(self, expert_out_bits, permuted_row_of, topk_weights, residual_in,
                                         gamma_bits, eps: float, s_enc: float,
                                         tokens: Optional[Sequence[int]] = None):
@@ -330,6 +344,10 @@ def finalize_only(*a, **kw):
 
 def nvfp4_quantize(*a, **kw):
     return default().nvfp4_quantize(*a, **kw)
+
+
+def nvfp4_encode(*a, **kw):
+    return default().nvfp4_encode(*a, **kw)
 
 
 def finalize_residual_rmsnorm_nvfp4(*a, **kw):

@@ -386,6 +386,21 @@ double mfr_oracle_e2m1_to_f64(uint8_t c)
     return ((c & 0x8u) ? -1.0 : 1.0) * k_e2m1_mag[c & 7];
 }
 
+/* The last three steps for one block of 16 elements whose scale is already
+ * chosen, sv being the value of its E4M3 byte: dec = sv / s_enc, enc = 1 / dec
+ * (0 for a zero scale), q_i = E2M1(y_i * enc), packed into 8 bytes. */
+static void nvfp4_encode_block(const float* yb, float sv, float s_enc, uint8_t* qb)
+{
+    float dec = sv / s_enc;
+    float enc = (sv == 0.0f) ? 0.0f : 1.0f / dec;
+    for (int j = 0; j < 16; j += 2) {
+        float p0 = yb[j] * enc, p1 = yb[j + 1] * enc;
+        uint8_t c0 = mfr_oracle_e2m1_from_f64((double)p0);
+        uint8_t c1 = mfr_oracle_e2m1_from_f64((double)p1);
+        qb[j / 2] = (uint8_t)(c0 | (c1 << 4));
+    }
+}
+
 /* Quantises n rows of width H (H a multiple of 16) as described above.
  * q_packed: n x H/2 bytes; sf: n x H/16 bytes. */
 void mfr_oracle_nvfp4_quantize(int64_t n, int64_t H, const float* y, float s_enc,
@@ -401,17 +416,24 @@ void mfr_oracle_nvfp4_quantize(int64_t n, int64_t H, const float* y, float s_enc
             float v = (amax / 6.0f) * s_enc;
             uint8_t s8 = mfr_oracle_e4m3_from_f64((double)v);
             float sv = (float)mfr_oracle_e4m3_to_f64(s8);
-            float dec = sv / s_enc;
-            float enc = (s8 == 0) ? 0.0f : 1.0f / dec;
             sf[i * (H / 16) + b] = s8;
-            for (int j = 0; j < 16; j += 2) {
-                float p0 = yb[j] * enc, p1 = yb[j + 1] * enc;
-                uint8_t c0 = mfr_oracle_e2m1_from_f64((double)p0);
-                uint8_t c1 = mfr_oracle_e2m1_from_f64((double)p1);
-                q_packed[i * (H / 2) + b * 8 + j / 2] = (uint8_t)(c0 | (c1 << 4));
-            }
+            nvfp4_encode_block(yb, sv, s_enc, q_packed + i * (H / 2) + b * 8);
         }
     }
+}
+
+/* The codes of n rows of width H for block scales that the caller chooses
+ * (sf: n x H/16 E4M3 bytes), by the same steps as mfr_oracle_nvfp4_quantize
+ * after its scale choice.  Used to check an implementation whose scale
+ * differs from the quantiser's only where the scale's own rounding decision
+ * is ambiguous: its codes must then be those of its scale. */
+void mfr_oracle_nvfp4_encode(int64_t n, int64_t H, const float* y, float s_enc,
+                             const uint8_t* sf, uint8_t* q_packed)
+{
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t b = 0; b < H / 16; ++b)
+            nvfp4_encode_block(y + i * H + b * 16, (float)mfr_oracle_e4m3_to_f64(sf[i * (H / 16) + b]),
+                               s_enc, q_packed + i * (H / 2) + b * 8);
 }
 
 /* The whole path with the NVFP4 epilogue: the residual as above, RMSNorm in

@@ -69,6 +69,9 @@ MUTATIONS = {
     "nibbles_swapped": [("(uint8_t)(c0 | (c1 << 4))", "(uint8_t)(c1 | (c0 << 4))")],
     "scale_not_rounded": [("            float sv = (float)mfr_oracle_e4m3_to_f64(s8);",
                            "            float sv = v;")],
+    "encode_ignores_the_given_scale": [
+        ("nvfp4_encode_block(y + i * H + b * 16, (float)mfr_oracle_e4m3_to_f64(sf[i * (H / 16) + b]),",
+         "nvfp4_encode_block(y + i * H + b * 16, 1.0f,")],
     "amax_over_8": [("            for (int j = 0; j < 16; ++j)\n                if (fabsf(yb[j]) > amax)",
                      "            for (int j = 0; j < 8; ++j)\n                if (fabsf(yb[j]) > amax)")],
     "expert_norm_gamma_dropped": [

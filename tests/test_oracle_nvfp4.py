@@ -96,3 +96,34 @@ def test_block_scale_properties(oracle_lib):
             assert np.all(err <= best + 1e-12)                # nearest representable
     q2, sf2 = oracle_lib.nvfp4_quantize((y * np.float32(4)).astype(np.float32), s_enc / 4)
     assert np.array_equal(q2, q) and np.array_equal(sf2, sf)
+
+
+def test_hand_worked_encode_at_given_scales(oracle_lib):
+    """The codes for block scales the caller chooses (the check of an
+    implementation whose scale decision may differ at a rounding boundary)."""
+    with open(os.path.join(GOLDEN, "nvfp4_encode_at_given_scales_hand_worked.json")) as f:
+        g = json.load(f)
+    y = np.array([g["y"]], dtype=np.float32)
+    sf = np.array([[int(b, 16) for b in g["scale_bytes"]]], dtype=np.uint8)
+    q = oracle_lib.nvfp4_encode(y, g["s_enc"], sf)
+    assert [f"{b:02X}" for b in q[0]] == g["expected_packed_bytes"]
+    want = [int(c, 16) for blk in g["expected_codes"] for c in blk]
+    assert [int(c) for c in unpack_e2m1(q)[0]] == want
+
+
+def test_encode_at_the_quantisers_own_scales_gives_its_codes(oracle_lib):
+    """At the scales the quantiser chose, encoding reproduces its codes; at
+    any scale every code is the nearest E2M1 value of y * s_enc / value(sf)."""
+    rng = np.random.default_rng(33)
+    y = (rng.standard_normal((5, 48)) * np.exp2(rng.integers(-4, 4, (5, 1)))).astype(np.float32)
+    s_enc = 448.0 * 6.0 / float(np.abs(y).max())
+    q, sf = oracle_lib.nvfp4_quantize(y, s_enc)
+    assert np.array_equal(oracle_lib.nvfp4_encode(y, s_enc, sf), q)
+    other = np.clip(sf.astype(np.int64) + rng.integers(-3, 4, sf.shape), 1, 0x7E).astype(np.uint8)
+    codes = unpack_e2m1(oracle_lib.nvfp4_encode(y, s_enc, other))
+    dec = (oracle_lib.e4m3_to_f64(other).astype(np.float32) / np.float32(s_enc)).astype(np.float32)
+    enc = (np.float32(1.0) / dec).astype(np.float32)
+    z = (y * np.repeat(enc, 16, axis=1)).astype(np.float64)
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    best = np.min(np.abs(np.abs(z)[..., None] - mags), axis=-1)
+    assert np.all(np.abs(oracle_lib.e2m1_to_f64(codes) - z) <= best + 1e-12)
