@@ -1,14 +1,11 @@
 """The NVFP4 epilogue (residual + RMSNorm, output quantised to NVFP4)
 against the oracle.
 
-The GPU computes the normalised value y in FP32 (rsqrtf, an FP32 sum of
-squares); the oracle computes it in double and rounds once to FP32, so the
-two y differ by a few units in the last place.  Both then take every
-quantisation decision (block scale, codes) with the same FP32 steps.  A
-decision can therefore only differ where the oracle's own decision flips
-when y moves by a few ulps: such blocks / elements are "ambiguous" (found by
-quantising y * (1 -/+ 2^-16) with the oracle) and are checked for validity
-instead of equality.  Everything else must be equal.
+The rules of the output check are those of nvfp4_check.check_nvfp4: scales
+and codes equal to the oracle's, except where the oracle's own decision
+flips when y moves by 2^-16 relative; there the kernel's scale must be one of
+the oracle's neighbouring decisions and its codes the oracle's codes at that
+scale.
 """
 import numpy as np
 import pytest
@@ -17,10 +14,10 @@ import torch
 import moe_finalize_residual_rmsnorm_gb300 as mfr
 import oracle
 import workloads as W
-from helpers import assert_residual_close, bf16_bits, f32
+from helpers import assert_residual_close, bf16_bits, f32, host_inputs, over_all_tokens
+from nvfp4_check import check_nvfp4
 
 pytestmark = pytest.mark.gpu
-REL = 2.0 ** -16
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,37 +56,6 @@ def run_nvfp4(inp, s_enc, **kw):
     for buf, fill in ((qb, 0xA5), (sb, 0x5A)):
         assert torch.all(buf[:G] == fill) and torch.all(buf[-G:] == fill), "write outside an NVFP4 output"
     return f32(rout), out_q.cpu().numpy(), out_sf.cpu().numpy(), plan
-
-
-def _mag(codes):
-    return np.where((codes & 7) == 0, 0, codes)       # +0 and -0 are the same value
-
-
-def check_nvfp4(y32, s_enc, q_gpu, sf_gpu, max_ambiguous=0.01):
-    q_o, sf_o = oracle.nvfp4_quantize(y32, s_enc)
-    lo = oracle.nvfp4_quantize((y32 * np.float32(1 - REL)).astype(np.float32), s_enc)
-    hi = oracle.nvfp4_quantize((y32 * np.float32(1 + REL)).astype(np.float32), s_enc)
-    n, H = y32.shape
-    c_o, c_g = oracle.unpack_e2m1(q_o), oracle.unpack_e2m1(q_gpu)
-    c_lo, c_hi = oracle.unpack_e2m1(lo[0]), oracle.unpack_e2m1(hi[0])
-    amb_block = (lo[1] != sf_o) | (hi[1] != sf_o)
-    amb_elem = (c_lo != c_o) | (c_hi != c_o) | np.repeat(amb_block, 16, axis=1)
-    sure_block = ~amb_block
-    assert np.array_equal(sf_gpu[sure_block], sf_o[sure_block]), "block scale differs away from a rounding boundary"
-    same_sf = np.repeat(sf_gpu == sf_o, 16, axis=1)
-    sure = ~amb_elem & same_sf
-    assert np.array_equal(_mag(c_g[sure]), _mag(c_o[sure])), "E2M1 code differs away from a rounding boundary"
-    assert amb_elem.mean() <= max_ambiguous
-    # every element, ambiguous or not: the GPU's code is a nearest E2M1 value of
-    # y * enc for the GPU's own block scale, within the y uncertainty
-    dec = (oracle.default().e4m3_to_f64(sf_gpu).astype(np.float32) / np.float32(s_enc)).astype(np.float32)
-    with np.errstate(divide="ignore"):
-        enc = np.where(sf_gpu == 0, np.float32(0), (np.float32(1) / dec).astype(np.float32))
-    z = y32.astype(np.float64) * np.repeat(enc, 16, axis=1)
-    vals = oracle.default().e2m1_to_f64(c_g)
-    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
-    best = np.min(np.abs(np.abs(z)[..., None] - mags), axis=-1)
-    assert np.all(np.abs(vals - z) <= best + np.abs(z) * 2 * REL + 1e-30)
 
 
 CASES = [
@@ -131,17 +97,26 @@ def test_nvfp4_repeats_bitwise_and_small_scales():
         check_nvfp4(y32, s_enc, a[1], a[2], max_ambiguous=0.05)
 
 
-def test_nvfp4_full_size_sampled_tokens():
+def test_nvfp4_full_size_every_token():
+    """Every token of the prefill call, with the oracle spread over the host
+    cores."""
     wl = W.PREFILL
     inp = W.make_inputs(wl, "cuda")
-    rng = np.random.default_rng(9)
-    tokens = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, size=30, replace=False)]))
-    x_o, y32 = _oracle_y32(inp, tokens=tokens)
     s_enc = float(np.float32(448.0 * 6.0 / 16.0))        # |y| stays well below 16 for these inputs
     res, q, sf, plan = run_nvfp4(inp, s_enc)
     assert plan.info()["variant_name"] == "stream"
-    assert_residual_close(res[tokens], x_o)
-    check_nvfp4(y32, s_enc, q[tokens], sf[tokens])
+    assert plan.get_status() == 0
+    h = host_inputs(inp)
+    del inp
+    torch.cuda.empty_cache()
+
+    def check(tk):
+        x_o, _ = oracle.weighted_residual(h["E"], h["idx"], h["w"], h["res"], tokens=tk)
+        y32 = oracle.rmsnorm_f64(x_o, h["gamma"], h["eps"]).astype(np.float32)
+        sl = slice(tk[0], tk[-1] + 1)
+        assert_residual_close(res[sl], x_o, what=f"residual_out tokens {tk[0]}..")
+        check_nvfp4(y32, s_enc, q[sl], sf[sl])
+    assert over_all_tokens(wl.T, check) == wl.T
 
 
 def test_nvfp4_argument_checks():
