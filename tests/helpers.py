@@ -1,5 +1,9 @@
-"""Shared test helpers: tolerances, comparisons, host copies.  No finalize
-arithmetic lives here."""
+"""Shared test helpers: tolerances, comparisons, host copies, and a runner
+that checks every token of a large call against the oracle on all host
+cores.  No finalize arithmetic lives here."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -43,6 +47,10 @@ def bf16_ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
 def assert_residual_close(got: np.ndarray, want: np.ndarray, what="residual_out"):
     got = np.asarray(got, dtype=np.float32)
     want = np.asarray(want, dtype=np.float32)
+    if got.shape != want.shape:
+        raise AssertionError(f"{what}: shape {got.shape} != {want.shape}")
+    if np.array_equal(got.view(np.uint32), want.view(np.uint32)):
+        return                                   # bit-equal: within any tolerance
     both_nan = np.isnan(got) & np.isnan(want)
     with np.errstate(invalid="ignore"):
         err = np.abs(got.astype(np.float64) - want.astype(np.float64))
@@ -55,6 +63,8 @@ def assert_residual_close(got: np.ndarray, want: np.ndarray, what="residual_out"
 
 
 def assert_out_close(got_bits: np.ndarray, want_bits: np.ndarray, what="out", ulp=OUT_ULP):
+    if got_bits.shape != want_bits.shape:
+        raise AssertionError(f"{what}: shape {got_bits.shape} != {want_bits.shape}")
     d = bf16_ulp_distance(got_bits, want_bits)
     if not np.all(d <= ulp):
         i = np.argwhere(~(d <= ulp))[0]
@@ -91,3 +101,59 @@ def oracle_expert_norm(inputs: dict, tokens=None):
     s, _ = oracle.expert_rmsnorm_f64(E & np.uint16(0x7FFF), idx, np.abs(w), g & np.uint16(0x7FFF),
                                      inputs["eps"], tokens=tokens)
     return out, y, s, bad
+
+
+# ---- every token of a large call, on all host cores ------------------------------
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def host_inputs(inputs: dict) -> dict:
+    """Host copies of a call's inputs, made once: bf16 as uint16 bits."""
+    return {"E": bf16_bits(inputs["expert_out"]), "idx": inputs["permuted_row_of"].cpu().numpy(),
+            "w": f32(inputs["topk_weights"]), "res": f32(inputs["residual"]), "gamma": bf16_bits(inputs["gamma"]),
+            "eps": inputs["eps"]}
+
+
+def over_all_tokens(T: int, check, chunk: int = 256, threads=None) -> int:
+    """Calls check(tokens) for consecutive chunks of [0, T) on a pool of host
+    threads (the oracle's C calls and NumPy's large-array operations release
+    the GIL) and re-raises the first failure.  Returns the tokens covered."""
+    chunks = [np.arange(a, min(a + chunk, T), dtype=np.int64) for a in range(0, T, chunk)]
+    with ThreadPoolExecutor(max_workers=threads or host_cores()) as ex:
+        for _ in ex.map(check, chunks):
+            pass
+    return int(sum(c.size for c in chunks))
+
+
+def check_every_token(h: dict, got_res: np.ndarray, got_out: np.ndarray, chunk: int = 256) -> int:
+    """The fused path's outputs (residual_out f32 [T, H], out bf16 bits
+    [T, H]) against the oracle, token by token over all T tokens."""
+    T = h["idx"].shape[0]
+
+    def check(tk):
+        want_res, want_out, bad = oracle.finalize_residual_rmsnorm(h["E"], h["idx"], h["w"], h["res"], h["gamma"],
+                                                                   h["eps"], tokens=tk)
+        assert bad == 0
+        assert_residual_close(got_res[tk[0]:tk[-1] + 1], want_res, what=f"residual_out tokens {tk[0]}..")
+        assert_out_close(got_out[tk[0]:tk[-1] + 1], want_out, what=f"out tokens {tk[0]}..")
+    return over_all_tokens(T, check, chunk)
+
+
+def check_every_token_finalize_only(h: dict, got_out: np.ndarray, chunk: int = 256) -> int:
+    """The plain finalize's bf16 output against the oracle's, bit for bit,
+    over all T tokens."""
+    T = h["idx"].shape[0]
+
+    def check(tk):
+        want, bad = oracle.finalize_only(h["E"], h["idx"], h["w"], tokens=tk)
+        assert bad == 0
+        got = got_out[tk[0]:tk[-1] + 1]
+        if not np.array_equal(got, want):
+            i = np.argwhere(got != want)[0]
+            raise AssertionError(f"finalize out differs at token {tk[0] + i[0]}, column {i[1]}")
+    return over_all_tokens(T, check, chunk)
