@@ -302,22 +302,34 @@ int moe_finalize_rmsnorm_bench_producer(const void* src, void* expert_out, int64
  * of MFR_NOALLOC_SLOTS ints (256 bytes), which every GPU that loads the
  * library keeps until the process exits.  `slot` picks the word this call
  * uses; a slot outside [0, MFR_NOALLOC_SLOTS) is rejected with
- * MFR_ERR_INVALID_ARG ("beyond the scratch").  The array keeps the last
- * call's contents, so every call first clears its word (an asynchronous
- * memset on `stream`).  Calls that use the same slot and overlap on the GPU
- * (different streams, or graph branches) race on that word: give concurrent
- * streams different slots.
+ * MFR_ERR_INVALID_ARG ("beyond the scratch").  The array keeps its contents
+ * from call to call: the set-up clears every word once, and after that a
+ * word is cleared only right after a call reads it back (host_status not
+ * NULL).  A call made with host_status NULL therefore leaves its bits in the
+ * word, and the next call on that slot that reads back reports them together
+ * with its own (the same sticky rule as a plan's status word and
+ * moe_finalize_rmsnorm_get_status).  No memset is queued ahead of the kernel,
+ * so nothing stands between the producing kernel and this one on the stream.
+ * Calls that use the same slot and overlap on the GPU (different streams, or
+ * graph branches) race on that word: give concurrent streams different slots.
  *
  * Set-up: the first call on a device (made with that device current) looks up
- * the array's device address with cudaGetSymbolAddress, queries the device
- * and sets the kernel's shared-memory attribute; make that first call before
- * any stream capture.  Later calls on the device reuse it.
+ * the array's device address with cudaGetSymbolAddress, clears the array
+ * (synchronously), queries the device and sets the kernel's shared-memory
+ * attribute; make that first call before any stream capture.  Later calls on
+ * the device reuse it.
  *
  * Arguments and layouts are those of moe_finalize_rmsnorm_run, with T, H, k
- * and R passed directly.  It always launches the persistent bulk-copy kernel
- * (MFR_VARIANT_STREAM geometry, PDL on).  If host_status is not NULL the call
- * waits for `stream` and stores the slot's MFR_STATUS_* bits there; if it is
- * NULL the call is fully asynchronous and the status is not reported. */
+ * and R passed directly; the library cannot check that the buffers are as
+ * large as (T, H, k, R) say.  It always launches the persistent bulk-copy
+ * kernel (MFR_VARIANT_STREAM geometry) with programmatic dependent launch on:
+ * the kernel reads permuted_row_of, topk_weights and gamma BEFORE waiting on
+ * the preceding kernel in the stream, and expert_out and residual_in after,
+ * so those three must not be written by a kernel that may still be running
+ * when this one starts (the rule of mfr_options.enable_pdl = 1).  If
+ * host_status is not NULL the call waits for `stream`, stores the slot's
+ * MFR_STATUS_* bits there and clears the word; if it is NULL the call is
+ * fully asynchronous and the bits stay in the word. */
 #define MFR_NOALLOC_SLOTS 64
 int moe_finalize_rmsnorm_run_noalloc(int64_t T, int64_t H, int k, int64_t R,
                                      const void* expert_out, const int32_t* permuted_row_of,

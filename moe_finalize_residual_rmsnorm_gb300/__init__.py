@@ -22,7 +22,7 @@ from .build import LIBRARY, build as _build_library
 __all__ = [
     "LIBRARY", "MFRError", "Plan", "FinalizePlan", "Nvfp4Plan", "ExpertNormPlan", "PlanInfo", "Options", "build", "load_library", "supports",
     "moe_finalize_residual_rmsnorm", "finalize_residual_rmsnorm_host", "exported_symbols",
-    "VARIANT_AUTO", "VARIANT_CLUSTER", "VARIANT_ROWS", "VARIANT_STREAM", "STATUS_BAD_INDEX",
+    "run_noalloc", "validate_fused_args", "VARIANT_AUTO", "VARIANT_CLUSTER", "VARIANT_ROWS", "VARIANT_STREAM", "STATUS_BAD_INDEX",
     "ERROR_CODES",
 ]
 
@@ -129,6 +129,36 @@ def supports(H: int, k: int) -> bool:
     return bool(load_library().moe_finalize_rmsnorm_supports(H, k))
 
 
+def validate_fused_args(T: int, H: int, k: int, R: int, expert_out, permuted_row_of, topk_weights, residual_in,
+                        residual_out, gamma, out) -> None:
+    """Checks the tensors of one fused call against (T, H, k, R): dtype and
+    shape of every tensor first, then contiguity, then that each is a CUDA
+    tensor.  Raises ValueError on the first mismatch.  The C ABI receives
+    bare pointers and cannot check sizes, so this is what keeps a wrongly
+    sized or strided tensor from being read or written out of bounds."""
+    import torch
+    want = [
+        ("expert_out", expert_out, torch.bfloat16, (R, H)),
+        ("permuted_row_of", permuted_row_of, torch.int32, (T, k)),
+        ("topk_weights", topk_weights, torch.float32, (T, k)),
+        ("residual_in", residual_in, torch.float32, (T, H)),
+        ("residual_out", residual_out, torch.float32, (T, H)),
+        ("gamma", gamma, torch.bfloat16, (H,)),
+        ("out", out, torch.bfloat16, (T, H)),
+    ]
+    for name, t, dt, shape in want:
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+        if t.dtype != dt or tuple(t.shape) != shape:
+            raise ValueError(f"{name}: expected {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
+    for name, t, _, _ in want:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    for name, t, _, _ in want:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
 def _ptr(t) -> Optional[int]:
     if t is None:
         return None
@@ -174,24 +204,8 @@ class Plan:
         return inf.as_dict()
 
     def _validate(self, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, out):
-        import torch
-        T, H, k, R = self.T, self.H, self.k, self.R
-        want = [
-            ("expert_out", expert_out, torch.bfloat16, (R, H)),
-            ("permuted_row_of", permuted_row_of, torch.int32, (T, k)),
-            ("topk_weights", topk_weights, torch.float32, (T, k)),
-            ("residual_in", residual_in, torch.float32, (T, H)),
-            ("residual_out", residual_out, torch.float32, (T, H)),
-            ("gamma", gamma, torch.bfloat16, (H,)),
-            ("out", out, torch.bfloat16, (T, H)),
-        ]
-        for name, t, dt, shape in want:
-            if t.dtype != dt or tuple(t.shape) != shape:
-                raise ValueError(f"{name}: expected {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
-            if not t.is_cuda:
-                raise ValueError(f"{name} must be a CUDA tensor")
-            if not t.is_contiguous():
-                raise ValueError(f"{name} must be contiguous")
+        validate_fused_args(self.T, self.H, self.k, self.R, expert_out, permuted_row_of, topk_weights, residual_in,
+                            residual_out, gamma, out)
 
     def run(self, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma,
             eps: float, out, stream=None, *, validate: bool = True) -> None:
@@ -357,11 +371,20 @@ NOALLOC_SLOTS = 64
 
 
 def run_noalloc(expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, eps: float, out,
-                *, slot: int = 0, report_status: bool = False, stream=None):
+                *, slot: int = 0, report_status: bool = False, stream=None, validate: bool = True):
     """Allocation-free call (C: moe_finalize_rmsnorm_run_noalloc): no plan, no
     device allocation; the status word is slot `slot` of the library's static
-    scratch.  Returns the status bits when report_status (the call then waits
-    for the stream), else None."""
+    scratch.  T, H, k and R are taken from permuted_row_of [T, k] and
+    expert_out [R, H], and every other tensor is checked against them
+    (validate_fused_args) before the C call.  Returns the status bits when
+    report_status (the call then waits for the stream), else None."""
+    if validate:
+        if permuted_row_of.dim() != 2 or expert_out.dim() != 2:
+            raise ValueError("permuted_row_of must be [T, k] and expert_out [R, H]")
+        T, k = permuted_row_of.shape
+        R, H = expert_out.shape
+        validate_fused_args(T, H, k, R, expert_out, permuted_row_of, topk_weights, residual_in, residual_out,
+                            gamma, out)
     lib = load_library()
     T, k = permuted_row_of.shape
     R, H = expert_out.shape

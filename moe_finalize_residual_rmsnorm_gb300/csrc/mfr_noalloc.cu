@@ -80,6 +80,15 @@ int setup_device(int dev, DeviceSetup* out) {
                 return MFR_ERR_CUDA;
             }
         }
+        // start every slot at zero once, here, so no memset sits between the
+        // producing kernel and a later call (it would cost the dependent
+        // launch its overlap); after that a word is cleared only when a call
+        // reads it back
+        if (cudaMemset(addr, 0, sizeof(int) * MFR_NOALLOC_SLOTS) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess) {
+            cudaGetLastError();
+            return MFR_ERR_CUDA;
+        }
         s.status = static_cast<int*>(addr);
         s.sms = sms;
         s.ring_budget = budget;
@@ -152,8 +161,6 @@ extern "C" int moe_finalize_rmsnorm_run_noalloc(
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* status = ds.status + slot;
-    // the array keeps the previous call's contents: this call's word starts at zero
-    if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) { cudaGetLastError(); return MFR_ERR_CUDA; }
 
     mfr::Params p{};
     p.expert_out = static_cast<const uint16_t*>(expert_out);
@@ -172,8 +179,11 @@ extern "C" int moe_finalize_rmsnorm_run_noalloc(
     if (mfr::stream_launch(p, l, s) != cudaSuccess) { cudaGetLastError(); return MFR_ERR_LAUNCH; }
 
     if (host_status) {
+        // read the word, then clear it behind the read, in stream order: the
+        // next call on this slot starts from zero without a memset of its own
         int h = 0;
         if (cudaMemcpyAsync(&h, status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess ||
             cudaStreamSynchronize(s) != cudaSuccess) {
             cudaGetLastError();
             return MFR_ERR_CUDA;

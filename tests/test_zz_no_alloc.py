@@ -3,9 +3,9 @@
 It serves callers that cannot allocate device memory (an engine that owns
 all device memory through its own pool, a host that may not call cudaMalloc
 on the request path): no plan, no allocation, the status word in the
-library's static device scratch.  Its outputs must equal those of the
-planned entry point (moe_finalize_rmsnorm_plan + _run) within the parity
-tolerances, on two calls in a row.
+library's static device scratch.  Its outputs must match the oracle within
+the parity tolerances on two calls in a row, and equal those of the planned
+entry point (moe_finalize_rmsnorm_plan + _run).
 
 This file is collected last on purpose, and also passes alone in a fresh
 process.
@@ -18,7 +18,7 @@ import torch
 
 import moe_finalize_residual_rmsnorm_gb300 as mfr
 import workloads as W
-from helpers import assert_out_close, assert_residual_close, bf16_bits, f32
+from helpers import assert_out_close, assert_residual_close, bf16_bits, f32, oracle_on
 
 pytestmark = pytest.mark.gpu
 
@@ -55,9 +55,11 @@ def _planned(inp):
 
 @pytest.mark.parametrize("wl", [W.TINY_REF, W.PREFILL.with_(T=1000), W.wide(64), W.STRESS.with_(T=300)],
                          ids=lambda w: f"{w.name}_T{w.T}")
-def test_noalloc_matches_the_planned_entry_point_twice(lib, wl):
+def test_noalloc_matches_the_oracle_twice(lib, wl):
     inp = W.make_inputs(wl, "cuda")
-    want_res, want_out = _planned(inp)
+    want_res, want_out, bad = oracle_on(inp)
+    assert bad == 0
+    plan_res, plan_out = _planned(inp)
     for call in range(2):
         rout = torch.full_like(inp["residual"], float("nan"))
         out = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -67,6 +69,9 @@ def test_noalloc_matches_the_planned_entry_point_twice(lib, wl):
         torch.cuda.synchronize()
         assert_residual_close(f32(rout), want_res)
         assert_out_close(bf16_bits(out), want_out)
+        # and the planned entry point's outputs, within the same tolerances
+        assert_residual_close(f32(rout), plan_res)
+        assert_out_close(bf16_bits(out), plan_out)
 
 
 def test_noalloc_reports_bad_indices_and_clears_its_word(lib):
@@ -80,8 +85,14 @@ def test_noalloc_reports_bad_indices_and_clears_its_word(lib):
     st = ctypes.c_int(0)
     assert _call_noalloc(lib, bad, rout, out, slot=5, status=st) == 0
     assert st.value & mfr.STATUS_BAD_INDEX
-    # the next call on the same slot starts from a cleared word
+    # the read-back cleared the word: the next call on the same slot starts from zero
     assert _call_noalloc(lib, inp, rout, out, slot=5, status=st) == 0
+    assert st.value == 0
+    # a call without read-back leaves its bits for the next call that reads back
+    assert _call_noalloc(lib, bad, rout, out, slot=6, status=None) == 0
+    assert _call_noalloc(lib, inp, rout, out, slot=6, status=st) == 0
+    assert st.value & mfr.STATUS_BAD_INDEX
+    assert _call_noalloc(lib, inp, rout, out, slot=6, status=st) == 0
     assert st.value == 0
 
 
@@ -108,9 +119,26 @@ def test_noalloc_allocates_nothing_through_torch(lib):
                         inp["gamma"], inp["eps"], out, slot=slot)
     torch.cuda.synchronize()
     assert torch.cuda.memory_stats()["allocation.all.allocated"] == before
-    want_res, want_out = _planned(inp)
-    assert np.array_equal(f32(rout).view(np.uint32), want_res.view(np.uint32))
+    want_res, want_out, _ = oracle_on(inp)
+    assert_residual_close(f32(rout), want_res)
     assert_out_close(bf16_bits(out), want_out)
+
+
+def test_noalloc_binding_rejects_wrong_tensors_before_the_call(lib):
+    """The C call cannot check buffer sizes; the binding refuses a wrongly
+    sized, typed or strided tensor before anything is launched."""
+    inp = W.make_inputs(W.decode(4), "cuda")
+    args = dict(expert_out=inp["expert_out"], permuted_row_of=inp["permuted_row_of"],
+                topk_weights=inp["topk_weights"], residual_in=inp["residual"],
+                residual_out=torch.empty_like(inp["residual"]), gamma=inp["gamma"], eps=inp["eps"],
+                out=torch.empty((4, 4096), dtype=torch.bfloat16, device="cuda"))
+    for name, bad in [("residual_out", torch.empty((3, 4096), dtype=torch.float32, device="cuda")),
+                      ("out", torch.empty((4, 4096), dtype=torch.float32, device="cuda")),
+                      ("residual_out", torch.empty((4096, 4), dtype=torch.float32, device="cuda").t()),
+                      ("gamma", inp["gamma"].cpu())]:
+        with pytest.raises(ValueError):
+            mfr.run_noalloc(**{**args, name: bad})
+    torch.cuda.synchronize()
 
 
 def test_noalloc_ring_fits_after_a_plan_set_the_kernel_attribute(lib):
@@ -119,7 +147,8 @@ def test_noalloc_ring_fits_after_a_plan_set_the_kernel_attribute(lib):
     must still launch after a plan has set the attribute."""
     wl = W.PREFILL.with_(T=400, k=5)
     inp = W.make_inputs(wl, "cuda")
-    want_res, want_out = _planned(inp)       # makes a plan: sets the attribute
+    _planned(inp)                            # makes a plan: sets the attribute
+    want_res, want_out, _ = oracle_on(inp)
     rout = torch.empty_like(inp["residual"])
     out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
     st = ctypes.c_int(-1)
