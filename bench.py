@@ -61,7 +61,11 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="prefill", choices=sorted(W.all_named()))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sweep", action="store_true", help="also time the decode and wide sweeps")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also time the full decode and wide sweeps (graph, stream loop, warm L2, other outputs)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the compact sweep of the metric (decode T<=8 against its floor, wide H=8192, "
+                         "stress) that the JSON line carries by default")
     ap.add_argument("--variants", action="store_true",
                     help="also time the plain finalize and the NVFP4 epilogue on the headline workload")
     ap.add_argument("--pdl-pairs", action="store_true",
@@ -395,8 +399,10 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "e2e": e2e,
     }
+    if not args.no_sweep and not args.tokens:
+        result["sweep"] = run_compact_sweep(mfr, device, args)
     if args.sweep:
-        result["sweep"] = run_sweep(mfr, device, args)
+        result["sweep_full"] = run_sweep(mfr, device, args)
     if args.pdl_pairs:
         result["pdl_pairs"] = run_pdl_pairs(mfr, device)
     if args.variants:
@@ -447,6 +453,162 @@ def run_e2e(args, plan, dev, nbytes, world, dist, device):
     return {"value": round(nbytes * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4),
             "steps": steps, "api": "moe_finalize_rmsnorm_run_host (C ABI), pinned host buffers, 2 streams"}
+
+
+def _quartiles(xs):
+    q = np.percentile(np.asarray(xs, dtype=np.float64), [25, 50, 75])
+    return float(q[1]), float(q[2] - q[0])
+
+
+def decode_against_floor(mfr, device, wl, args, replays=25, ncalls=4096):
+    """One decode size, the call and its launch floor measured in the same run.
+
+    Both are CUDA graphs of `ncalls` launches on one stream: the call graph
+    cycles through enough input/output sets to exceed 3x L2 (each call reads
+    cold data), the floor graph holds the same number of empty kernels with
+    the plan's exact launch geometry and PDL attribute
+    (moe_finalize_rmsnorm_launch_floor).  The two graphs are replayed
+    alternately, `replays` times each, so clock or neighbour drift hits both
+    alike; the row gives median and interquartile range of each and the SM
+    clock sampled meanwhile.  The target is
+    us_per_call <= 2 * (floor_us + bytes / 8 TB/s), from these medians."""
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    nbytes = W.algorithmic_bytes(wl.T, wl.H, wl.k)
+    nsets = int(min(ncalls, max(2, -(-3 * l2 // max(nbytes, 1)))))
+    base = W.make_inputs(wl, device)
+    T, H, k, R = wl.T, wl.H, wl.k, wl.R
+    E = base["expert_out"].unsqueeze(0).expand(nsets, R, H).contiguous()
+    idx = base["permuted_row_of"].unsqueeze(0).expand(nsets, T, k).contiguous()
+    w = base["topk_weights"].unsqueeze(0).expand(nsets, T, k).contiguous()
+    res = base["residual"].unsqueeze(0).expand(nsets, T, H).contiguous()
+    rout = torch.empty_like(res)
+    out = torch.empty((nsets, T, H), dtype=torch.bfloat16, device=device)
+    g, eps = base["gamma"], base["eps"]
+    plan = mfr.Plan(T, H, k, R, enable_pdl=not args.no_pdl)
+    stream = torch.cuda.Stream(device)
+    graphs = {}
+    with torch.cuda.stream(stream):
+        for kind in ("call", "floor"):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(ncalls):
+                    if kind == "floor":
+                        plan.launch_floor(stream)
+                    else:
+                        j = i % nsets
+                        plan.run(E[j], idx[j], w[j], res[j], rout[j], g, eps, out[j], stream, validate=False)
+            graph.replay()
+            graphs[kind] = graph
+        stream.synchronize()
+        times = {"call": [], "floor": []}
+        with ClockSampler(device.index) as clocks:
+            clocks.wait_first()
+            for _ in range(replays):
+                for kind in ("call", "floor"):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    graphs[kind].replay()
+                    b.record(stream)
+                    b.synchronize()
+                    times[kind].append(a.elapsed_time(b) * 1e3 / ncalls)
+    if plan.get_status(stream) != 0:
+        raise RuntimeError(f"the device status word reported an error during {wl.name}")
+    us, us_iqr = _quartiles(times["call"])
+    fl, fl_iqr = _quartiles(times["floor"])
+    ck = clocks.summary()
+    info = plan.info()
+    target = 2 * (fl + nbytes / 8e12 * 1e6)
+    del graphs, E, idx, w, res, rout, out, base
+    torch.cuda.empty_cache()
+    return {"workload": wl.name, "T": T, "H": H, "us_per_call": round(us, 3), "us_iqr": round(us_iqr, 3),
+            "floor_us": round(fl, 3), "floor_iqr": round(fl_iqr, 3), "vs_2x_floor": round(us / target, 3),
+            "sm_mhz": ck["sm_mhz"], "us_x_mhz": round(us * ck["sm_mhz"], 1) if ck["sm_mhz"] else None,
+            "clock_reasons": ck["reasons"], "replays": replays, "graph_calls": ncalls, "sets": nsets,
+            "variant": info["variant_name"], "cluster": info["cluster"]}
+
+
+def bandwidth_row(mfr, device, wl, args, steps, peak, repeat_check=False):
+    """µs/call, GB/s and fraction of the measured copy bandwidth for one
+    workload, timed like the headline step (CUDA events around `steps`
+    calls on one stream; input/output sets rotate so that together they
+    exceed 3x L2 and no call starts with its data in L2).  With
+    repeat_check, two further calls into fresh buffers must reproduce the
+    first call's outputs bit for bit."""
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    T, H, k, R = wl.T, wl.H, wl.k, wl.R
+    nbytes = W.algorithmic_bytes(T, H, k)
+    nsets = int(min(16, max(2, -(-3 * l2 // nbytes))))
+    sets = []
+    for s in range(nsets):
+        d = W.make_inputs(wl.with_(seed=wl.seed * 16 + s), device) if s < 2 or nbytes > l2 else None
+        if d is None:   # small calls: further sets are copies of the first two (what matters is the address)
+            d = {key: (v.clone() if torch.is_tensor(v) else v) for key, v in sets[s % 2].items()
+                 if key not in ("residual_out", "out")}
+        d["residual_out"] = torch.empty_like(d["residual"])
+        d["out"] = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        sets.append(d)
+    plan = mfr.Plan(T, H, k, R, enable_pdl=not args.no_pdl)
+    stream = torch.cuda.Stream(device)
+
+    def step(i):
+        d = sets[i % nsets]
+        plan.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["residual"], d["residual_out"],
+                 d["gamma"], d["eps"], d["out"], stream, validate=False)
+
+    for i in range(max(3, nsets)):
+        step(i)
+    stream.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index) as clocks:
+        clocks.wait_first()
+        a.record(stream)
+        for i in range(steps):
+            step(i)
+        b.record(stream)
+        b.synchronize()
+    us = a.elapsed_time(b) * 1e3 / steps
+    info = plan.info()
+    row = {"workload": wl.name, "T": T, "H": H, "us_per_call": round(us, 2),
+           "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1), "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4),
+           "bytes_per_call": nbytes, "steps": steps, "sets": nsets, "variant": info["variant_name"],
+           "grid": info["grid_x"], "sm_mhz": clocks.summary()["sm_mhz"], "clock_reasons": clocks.summary()["reasons"]}
+    if repeat_check:
+        d = sets[0]
+        step(0)
+        stream.synchronize()
+        ok = True
+        for _ in range(2):
+            r2, o2 = torch.empty_like(d["residual_out"]), torch.empty_like(d["out"])
+            plan.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["residual"], r2, d["gamma"],
+                     d["eps"], o2, stream, validate=False)
+            stream.synchronize()
+            ok = ok and torch.equal(r2.view(torch.int32), d["residual_out"].view(torch.int32)) and \
+                torch.equal(o2.view(torch.int16), d["out"].view(torch.int16))
+            del r2, o2
+        row["bitwise_repeat"] = bool(ok)
+    if plan.get_status(stream) != 0:
+        raise RuntimeError(f"the device status word reported an error during {wl.name}")
+    del sets
+    torch.cuda.empty_cache()
+    return row
+
+
+def run_compact_sweep(mfr, device, args):
+    """The metric's sweep in a form short enough for every run: decode
+    T = 1, 2, 4, 8 at H = 4096 against the launch-plus-one-HBM-pass floor
+    (decode_against_floor), the mid size T = 512 and T = 4096, 8192 at
+    H = 8192, and the stress configuration T = 32768, H = 8192 with its
+    bitwise-repeat check (bandwidth_row)."""
+    peak, _ = measured_peak()
+    t0 = time.perf_counter()
+    decode = [decode_against_floor(mfr, device, W.decode(t), args) for t in (1, 2, 4, 8)]
+    bandwidth = [bandwidth_row(mfr, device, W.wide(512), args, 400, peak),
+                 bandwidth_row(mfr, device, W.wide(4096), args, 60, peak),
+                 bandwidth_row(mfr, device, W.wide(8192), args, 40, peak),
+                 bandwidth_row(mfr, device, W.STRESS, args, 12, peak, repeat_check=True)]
+    return {"decode": decode, "bandwidth": bandwidth, "peak_gbs": peak,
+            "decode_target": "us_per_call <= 2 * (floor_us + bytes / 8 TB/s), medians of alternating replays",
+            "seconds": round(time.perf_counter() - t0, 1)}
 
 
 def run_sweep(mfr, device, args):

@@ -39,6 +39,15 @@ def test_gpu_arm_prints_the_contract_line():
     e = d["e2e"]
     assert e["unit"] == "GB/s" and e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    # the compact sweep of the metric rides on every default line
+    sw = d["sweep"]
+    assert [r["T"] for r in sw["decode"]] == [1, 2, 4, 8]
+    for r in sw["decode"]:
+        assert r["H"] == 4096 and r["replays"] >= 21 and r["floor_us"] > 0 and r["us_per_call"] > r["floor_us"]
+        assert abs(r["vs_2x_floor"] - r["us_per_call"] / (2 * (r["floor_us"] + r["T"] * 106560 / 8e12 * 1e6))) < 2e-3
+    assert [(r["T"], r["H"]) for r in sw["bandwidth"]] == [(512, 8192), (4096, 8192), (8192, 8192), (32768, 8192)]
+    assert all(0 < r["frac"] < 1.5 for r in sw["bandwidth"])
+    assert sw["bandwidth"][-1]["bitwise_repeat"] is True
     ref = run_bench("--impl", "reference", "--workload", "decode_T8", "--steps", "3", "--warmup", "3",
                     "--cpu-seconds", "0.05")
     shared = {k: v for k, v in ref["config"].items() if k != "bytes_per_call"}
