@@ -461,17 +461,33 @@ def _quartiles(xs):
 
 
 def decode_against_floor(mfr, device, wl, args, replays=25, ncalls=4096):
-    """One decode size, the call and its launch floor measured in the same run.
+    """One decode size: the call, its launch floor and its one-pass floors,
+    measured in the same run.
 
-    Both are CUDA graphs of `ncalls` launches on one stream: the call graph
-    cycles through enough input/output sets to exceed 3x L2 (each call reads
-    cold data), the floor graph holds the same number of empty kernels with
-    the plan's exact launch geometry and PDL attribute
-    (moe_finalize_rmsnorm_launch_floor).  The two graphs are replayed
-    alternately, `replays` times each, so clock or neighbour drift hits both
-    alike; the row gives median and interquartile range of each and the SM
-    clock sampled meanwhile.  The target is
-    us_per_call <= 2 * (floor_us + bytes / 8 TB/s), from these medians."""
+    Every figure is a CUDA graph of `ncalls` launches on one stream, per
+    launch.  The call graph cycles through enough input/output sets to
+    exceed 3x L2, so each call reads cold data.  The floor graphs use the
+    plan's exact launch geometry and PDL attribute:
+      floor_us             the empty kernel (moe_finalize_rmsnorm_launch_floor),
+                           timed on the second of two back-to-back replays: the
+                           launch path in its steady state (the launch floor
+                           the decode target is defined on)
+      floor_after_call_us  the first of those two replays, right after a call
+                           replay: launches of a graph that follows data-moving
+                           work run slower (context)
+      load_floor_us, store_floor_us  the empty kernel plus only the call's
+                           loads (LOAD), or only its stores (STORE)
+      pass_floor_us        the empty kernel plus the call's loads and stores
+                           over the same cold input sets, no arithmetic
+                           (moe_finalize_rmsnorm_launch_floor_work, LOAD|STORE):
+                           launch plus one pass over the call's bytes, measured
+      pass_exchange_floor_us  the same with one cluster barrier between loads
+                           and stores (LOAD|EXCHANGE|STORE)
+    One round replays call, floor, floor, load, store, pass, pass + exchange; `replays`
+    rounds; median and interquartile range of each; the SM clock is sampled
+    meanwhile.  The target is us_per_call <= 2 * (floor_us + bytes / 8 TB/s)
+    (vs_2x_floor, same-run medians); vs_2x_pass_floor compares with twice the
+    measured one-pass floor instead."""
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     nbytes = W.algorithmic_bytes(wl.T, wl.H, wl.k)
     nsets = int(min(ncalls, max(2, -(-3 * l2 // max(nbytes, 1)))))
@@ -486,42 +502,59 @@ def decode_against_floor(mfr, device, wl, args, replays=25, ncalls=4096):
     g, eps = base["gamma"], base["eps"]
     plan = mfr.Plan(T, H, k, R, enable_pdl=not args.no_pdl)
     stream = torch.cuda.Stream(device)
+    work = {"load": mfr.FLOOR_LOAD, "store": mfr.FLOOR_STORE, "pass": mfr.FLOOR_LOAD | mfr.FLOOR_STORE,
+            "pass_exchange": mfr.FLOOR_LOAD | mfr.FLOOR_EXCHANGE | mfr.FLOOR_STORE}
     graphs = {}
     with torch.cuda.stream(stream):
-        for kind in ("call", "floor"):
+        for kind in ("call", "floor", "load", "store", "pass", "pass_exchange"):
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 for i in range(ncalls):
+                    j = i % nsets
                     if kind == "floor":
                         plan.launch_floor(stream)
-                    else:
-                        j = i % nsets
+                    elif kind == "call":
                         plan.run(E[j], idx[j], w[j], res[j], rout[j], g, eps, out[j], stream, validate=False)
+                    else:
+                        plan.launch_floor_work(work[kind], E[j], idx[j], res[j], rout[j], out[j], stream)
             graph.replay()
             graphs[kind] = graph
         stream.synchronize()
-        times = {"call": [], "floor": []}
+
+        def timed(kind):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graphs[kind].replay()
+            b.record(stream)
+            b.synchronize()
+            return a.elapsed_time(b) * 1e3 / ncalls
+
+        times = {"call": [], "floor_after_call": [], "floor": [], "load": [], "store": [], "pass": [],
+                 "pass_exchange": []}
         with ClockSampler(device.index) as clocks:
             clocks.wait_first()
             for _ in range(replays):
-                for kind in ("call", "floor"):
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    graphs[kind].replay()
-                    b.record(stream)
-                    b.synchronize()
-                    times[kind].append(a.elapsed_time(b) * 1e3 / ncalls)
+                times["call"].append(timed("call"))
+                times["floor_after_call"].append(timed("floor"))
+                times["floor"].append(timed("floor"))
+                for kind in ("load", "store", "pass", "pass_exchange"):
+                    times[kind].append(timed(kind))
     if plan.get_status(stream) != 0:
         raise RuntimeError(f"the device status word reported an error during {wl.name}")
-    us, us_iqr = _quartiles(times["call"])
-    fl, fl_iqr = _quartiles(times["floor"])
+    q = {kind: _quartiles(v) for kind, v in times.items()}
+    us, fl, ps = q["call"][0], q["floor"][0], q["pass"][0]
     ck = clocks.summary()
     info = plan.info()
-    target = 2 * (fl + nbytes / 8e12 * 1e6)
     del graphs, E, idx, w, res, rout, out, base
     torch.cuda.empty_cache()
-    return {"workload": wl.name, "T": T, "H": H, "us_per_call": round(us, 3), "us_iqr": round(us_iqr, 3),
-            "floor_us": round(fl, 3), "floor_iqr": round(fl_iqr, 3), "vs_2x_floor": round(us / target, 3),
+    return {"workload": wl.name, "T": T, "H": H, "us_per_call": round(us, 3), "us_iqr": round(q["call"][1], 3),
+            "floor_us": round(fl, 3), "floor_iqr": round(q["floor"][1], 3),
+            "vs_2x_floor": round(us / (2 * (fl + nbytes / 8e12 * 1e6)), 3),
+            "floor_after_call_us": round(q["floor_after_call"][0], 3),
+            "load_floor_us": round(q["load"][0], 3), "store_floor_us": round(q["store"][0], 3),
+            "pass_floor_us": round(ps, 3), "pass_floor_iqr": round(q["pass"][1], 3),
+            "pass_exchange_floor_us": round(q["pass_exchange"][0], 3),
+            "vs_2x_pass_floor": round(us / (2 * ps), 3),
             "sm_mhz": ck["sm_mhz"], "us_x_mhz": round(us * ck["sm_mhz"], 1) if ck["sm_mhz"] else None,
             "clock_reasons": ck["reasons"], "replays": replays, "graph_calls": ncalls, "sets": nsets,
             "variant": info["variant_name"], "cluster": info["cluster"]}

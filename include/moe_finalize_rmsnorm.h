@@ -228,6 +228,34 @@ int moe_finalize_rmsnorm_get_status(mfr_plan_t plan, void* stream, int* device_s
  * floor of a call.  Touches no memory.  T == 0 is a no-op. */
 int moe_finalize_rmsnorm_launch_floor(mfr_plan_t plan, void* stream);
 
+/* The launch-plus-one-pass floor of a call: the same empty kernel with the
+ * plan's exact launch geometry and dependent-launch protocol (including the
+ * slot-index reads, the cluster barrier and the L2 prefetch that precede the
+ * wait), plus, after the wait, the parts of the call's data movement that
+ * `work` selects, with no arithmetic:
+ *   MFR_FLOOR_LOAD      each thread loads its 16-byte chunks of the k slot
+ *                       rows of expert_out and of residual_in (the call's reads)
+ *   MFR_FLOOR_EXCHANGE  one barrier over the token's cluster of CTAs (a CTA
+ *                       barrier for one-CTA plans): the least a cross-CTA
+ *                       reduction costs
+ *   MFR_FLOOR_STORE     each thread stores its chunks of residual_out and out
+ *                       (the call's writes; their contents are unspecified)
+ * work = 0 is moe_finalize_rmsnorm_launch_floor plus the prologue's reads.
+ * Benchmarks time it beside a call to split a small call's time into launch,
+ * data movement, exchange and the kernel's own work.  Only plans made by
+ * moe_finalize_rmsnorm_plan whose variant is MFR_VARIANT_CLUSTER or
+ * MFR_VARIANT_ROWS (MFR_ERR_UNSUPPORTED_SHAPE otherwise).  Pointers, sizes,
+ * alignment and overlap rules are those of moe_finalize_rmsnorm_run;
+ * permuted_row_of is always read, the others only when `work` needs them
+ * (NULL allowed otherwise).  work outside [0, 7] is MFR_ERR_INVALID_ARG.  An
+ * index outside [0, R) is skipped (no status bit).  T == 0 is a no-op. */
+#define MFR_FLOOR_LOAD     1
+#define MFR_FLOOR_EXCHANGE 2
+#define MFR_FLOOR_STORE    4
+int moe_finalize_rmsnorm_launch_floor_work(mfr_plan_t plan, int work, const void* expert_out,
+                                           const int32_t* permuted_row_of, const float* residual_in,
+                                           float* residual_out, void* out, void* stream);
+
 /* Failure-path self test.  Enqueues one thread that waits on an on-chip
  * barrier with the same bounded-wait routine every kernel of the library uses
  * (each of their waits gives up after about 2 s and sets MFR_STATUS_TIMEOUT),

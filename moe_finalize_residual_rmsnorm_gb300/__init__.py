@@ -33,6 +33,7 @@ ERROR_CODES = {
 }
 STATUS_BAD_INDEX = 1
 STATUS_TIMEOUT = 2
+FLOOR_LOAD, FLOOR_EXCHANGE, FLOOR_STORE = 1, 2, 4
 VARIANT_AUTO, VARIANT_CLUSTER, VARIANT_ROWS, VARIANT_STREAM = 0, 1, 2, 3
 VARIANT_NAMES = {VARIANT_CLUSTER: "cluster", VARIANT_ROWS: "rows", VARIANT_STREAM: "stream"}
 
@@ -71,6 +72,7 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_get_status": (_I, [_VP, _VP, ctypes.POINTER(_I)]),
     "moe_finalize_rmsnorm_plan_info": (_I, [_VP, ctypes.POINTER(PlanInfo)]),
     "moe_finalize_rmsnorm_launch_floor": (_I, [_VP, _VP]),
+    "moe_finalize_rmsnorm_launch_floor_work": (_I, [_VP, _I, _VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_finalize_rmsnorm_wait_selftest": (_I, [_VP, ctypes.c_int64, ctypes.c_int, _VP]),
     "moe_finalize_rmsnorm_bench_producer": (_I, [_VP, _VP, _I64, _I64, ctypes.c_longlong, _I, _VP]),
     "moe_finalize_rmsnorm_host_workspace_bytes": (_I64, [_VP]),
@@ -237,6 +239,15 @@ class Plan:
         """Enqueues the empty kernel with this plan's launch geometry."""
         _check(self._lib.moe_finalize_rmsnorm_launch_floor(self._h, _stream_handle(stream)),
                "moe_finalize_rmsnorm_launch_floor")
+
+    def launch_floor_work(self, work: int, expert_out=None, permuted_row_of=None, residual_in=None,
+                          residual_out=None, out=None, stream=None) -> None:
+        """Enqueues the empty kernel with this plan's launch geometry plus the
+        call's loads, a cluster barrier and/or its stores (FLOOR_* bits;
+        C: moe_finalize_rmsnorm_launch_floor_work)."""
+        _check(self._lib.moe_finalize_rmsnorm_launch_floor_work(
+            self._h, int(work), _ptr(expert_out), _ptr(permuted_row_of), _ptr(residual_in), _ptr(residual_out),
+            _ptr(out), _stream_handle(stream)), "moe_finalize_rmsnorm_launch_floor_work")
 
     def host_workspace_bytes(self) -> int:
         return int(self._lib.moe_finalize_rmsnorm_host_workspace_bytes(self._h))

@@ -639,6 +639,60 @@ int moe_finalize_rmsnorm_launch_floor(mfr_plan_t plan, void* stream) {
     return MFR_OK;
 }
 
+int moe_finalize_rmsnorm_launch_floor_work(mfr_plan_t plan, int work, const void* expert_out,
+                                           const int32_t* permuted_row_of, const float* residual_in,
+                                           float* residual_out, void* out, void* stream) {
+    g_last_error[0] = '\0';
+    if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
+    if (work < 0 || work > (MFR_FLOOR_LOAD | MFR_FLOOR_EXCHANGE | MFR_FLOOR_STORE))
+        return fail(MFR_ERR_INVALID_ARG, "work must be a combination of the MFR_FLOOR_* bits (got %d)", work);
+    if (!plan->fused || plan->fp4 || plan->expert_norm)
+        return fail(MFR_ERR_INVALID_ARG, "the work floor takes plans made by moe_finalize_rmsnorm_plan");
+    if (plan->launch.variant == MFR_VARIANT_STREAM)
+        return fail(MFR_ERR_UNSUPPORTED_SHAPE, "the work floor covers the cluster and one-CTA-per-token variants");
+    const int64_t T = plan->T, H = plan->H, R = plan->R;
+    const int k = plan->k;
+    if (T == 0) return MFR_OK;
+    const bool load = work & MFR_FLOOR_LOAD, store = work & MFR_FLOOR_STORE;
+    if (!permuted_row_of || (load && (!residual_in || (R > 0 && !expert_out))) ||
+        (store && (!residual_out || !out)))
+        return fail(MFR_ERR_INVALID_ARG, "a pointer the requested work needs is NULL");
+    if (!aligned(permuted_row_of, 4) || (load && (!aligned(expert_out, 16) || !aligned(residual_in, 16))) ||
+        (store && (!aligned(residual_out, 16) || !aligned(out, 16))))
+        return fail(MFR_ERR_MISALIGNED, "misaligned pointer");
+    const size_t n_res = static_cast<size_t>(T * H) * 4, n_out = static_cast<size_t>(T * H) * 2;
+    const size_t n_e = static_cast<size_t>(R * H) * 2, n_tk = static_cast<size_t>(T * k) * 4;
+    if (store && (overlaps(residual_out, n_res, out, n_out) || overlaps(out, n_out, permuted_row_of, n_tk) ||
+                  overlaps(residual_out, n_res, permuted_row_of, n_tk) ||
+                  (load && (overlaps(out, n_out, expert_out, n_e) || overlaps(out, n_out, residual_in, n_res) ||
+                            overlaps(residual_out, n_res, expert_out, n_e) ||
+                            (residual_out != residual_in && overlaps(residual_out, n_res, residual_in, n_res))))))
+        return fail(MFR_ERR_INVALID_ARG, "an output overlaps another argument");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { cudaGetLastError(); return fail_cuda(MFR_ERR_CUDA, "cudaGetDevice", e); }
+    if (dev != plan->device)
+        return fail(MFR_ERR_INVALID_ARG, "current device %d is not the plan's device %d", dev, plan->device);
+    mfr::Params p{};
+    p.expert_out = static_cast<const uint16_t*>(expert_out);
+    p.permuted_row_of = permuted_row_of;
+    p.residual_in = residual_in;
+    p.residual_out = residual_out;
+    p.out = static_cast<uint16_t*>(out);
+    p.status = plan->d_status;
+    p.T = T;
+    p.R = R;
+    p.H = static_cast<int>(H);
+    p.k = k;
+    p.early_trigger = plan->launch.early_trigger;
+    e = mfr::floor_work_launch(p, plan->launch, work, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail_cuda(MFR_ERR_LAUNCH, "floor kernel launch", e);
+    }
+    return MFR_OK;
+}
+
 int moe_finalize_rmsnorm_plan_info(mfr_plan_t plan, mfr_plan_info* info) {
     if (!plan || !info) return fail(MFR_ERR_INVALID_ARG, "plan and info must not be NULL");
     const mfr::Launch& l = plan->launch;

@@ -62,6 +62,9 @@ cudaError_t rows_max_active_clusters(const Launch& l, int* n);
 cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s);
 // An empty kernel with the plan's launch geometry (for the launch floor).
 cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s);
+// The plan's launch geometry and protocol plus the call's loads, a cluster
+// barrier and/or its stores (MFR_FLOOR_* bits), no arithmetic.
+cudaError_t floor_work_launch(const Params& p, const Launch& l, int work, cudaStream_t s);
 // One bounded wait that runs out unless `arrive` (tests of the failure path).
 cudaError_t wait_selftest_launch(int* status, long long limit, int arrive, cudaStream_t s);
 

@@ -368,6 +368,114 @@ __global__ void floor_kernel(int* status) {
     if (status == nullptr && threadIdx.x == 0x7FFFFFFF) *status = 0;  // never taken; keeps the argument
 }
 
+// The launch-plus-one-pass floor of a fused plan: the plan's exact launch
+// geometry and dependent-launch protocol (trigger, cluster barrier arrived at
+// entry and completed before the wait, slot indices read and the CTA's row
+// and residual segments, and for the smallest calls its output lines,
+// prefetched into L2 before the wait), then, by the
+// bits of `work`, the call's data movement without its arithmetic:
+//   MFR_FLOOR_LOAD      every thread loads its 16-byte chunks of the k slot
+//                       rows and of the residual (the call's reads)
+//   MFR_FLOOR_EXCHANGE  one cluster-wide barrier (a CTA barrier without a
+//                       cluster): the least a cross-CTA reduction can cost
+//   MFR_FLOOR_STORE     every thread stores its chunks of residual_out (the
+//                       residual it loaded) and out (the XOR of its row
+//                       chunks): the call's writes
+// Benchmarks time it beside a call to split the call's time into launch,
+// data movement, exchange and the kernel's own work.
+constexpr int kFloorPrefetchOut = 8;   // internal bit: the plan prefetches its output lines
+
+template <int CPT>
+__global__ void __launch_bounds__(kRowsMaxThreads)
+floor_work_kernel(const Params p, const int csize, const int work)
+{
+    const int tid = threadIdx.x;
+    const int nthreads = blockDim.x;
+    const int64_t t = blockIdx.x / csize;
+    const int rank = static_cast<int>(blockIdx.x - t * csize);
+    const int nck = (p.H >> 3) / csize;
+    const int64_t col0 = static_cast<int64_t>(rank) * nck * 8;
+    const bool cluster = csize > 1;
+    const bool load = work & MFR_FLOOR_LOAD, store = work & MFR_FLOOR_STORE;
+    __shared__ int s_row[kMaxK];
+
+    if (p.early_trigger) pdl_launch_dependents();
+    if (cluster) cg::this_cluster().barrier_arrive();
+    if (tid < p.k) {
+        const int32_t r = p.permuted_row_of[t * p.k + tid];
+        s_row[tid] = (r >= 0 && static_cast<int64_t>(r) < p.R) ? r : -1;
+    }
+    __syncthreads();
+    if (load) {
+        if (tid < p.k && s_row[tid] >= 0)
+            prefetch_l2_bulk(p.expert_out + static_cast<int64_t>(s_row[tid]) * p.H + col0,
+                             static_cast<uint32_t>(nck) * 16u);
+        else if (tid == kMaxK)
+            prefetch_l2_bulk(p.residual_in + t * p.H + col0, static_cast<uint32_t>(nck) * 32u);
+    }
+    if (store && (work & kFloorPrefetchOut)) {   // as the plan's kernel does for the smallest calls
+        if (tid == kMaxK + 1)
+            prefetch_l2_bulk(p.residual_out + t * p.H + col0, static_cast<uint32_t>(nck) * 32u);
+        else if (tid == kMaxK + 2)
+            prefetch_l2_bulk(p.out + t * p.H + col0, static_cast<uint32_t>(nck) * 16u);
+    }
+    int rr[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) rr[j] = (j < p.k) ? s_row[j] : -1;
+    if (cluster) cg::this_cluster().barrier_wait();
+    pdl_wait();
+
+    float4 ra[CPT], rb[CPT];
+    uint4 fold[CPT];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        ra[i] = rb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        fold[i] = make_uint4(0, 0, 0, 0);
+    }
+    if (load) {
+        const float* res_in = p.residual_in + t * p.H + col0;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int c = tid + i * nthreads;
+            const int cc = c < nck ? c : 0;
+            ra[i] = ld_once_f4(res_in + cc * 8);
+            rb[i] = ld_once_f4(res_in + cc * 8 + 4);
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (rr[j] < 0) continue;   // the same for every thread
+            const uint16_t* row = p.expert_out + static_cast<int64_t>(rr[j]) * p.H + col0;
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                const int c = tid + i * nthreads;
+                const uint4 v = ld_stream_u4(row + (c < nck ? c : 0) * 8);
+                fold[i].x ^= v.x; fold[i].y ^= v.y; fold[i].z ^= v.z; fold[i].w ^= v.w;
+            }
+        }
+    }
+    if (!p.early_trigger) pdl_launch_dependents();
+    if (work & MFR_FLOOR_EXCHANGE) {
+        if (cluster) cg::this_cluster().sync();
+        else __syncthreads();
+    }
+    if (store) {
+        float* res_out = p.residual_out + t * p.H + col0;
+        uint16_t* out = p.out + t * p.H + col0;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int c = tid + i * nthreads;
+            if (c < nck) {
+                st_f4(res_out + c * 8, ra[i]);
+                st_f4(res_out + c * 8 + 4, rb[i]);
+                st_u4(out + c * 8, fold[i]);
+            }
+        }
+    } else if (load && p.T < 0) {
+        // never taken (T >= 1 here): keeps the loaded values live without a store
+        *p.status = static_cast<int>(fold[0].x ^ __float_as_uint(ra[0].x));
+    }
+}
+
 // One thread waits, with the kernels' bounded-wait helper, on an mbarrier
 // that gets its one arrival only if `arrive`; a wait that runs out sets
 // MFR_STATUS_TIMEOUT.  Exercises the failure path without faulting anything.
@@ -402,6 +510,21 @@ cudaError_t floor_launch(int* status, const Launch& l, cudaStream_t s) {
     cudaLaunchAttribute attrs[2];
     fill_config(cfg, attrs, l, s);
     return cudaLaunchKernelEx(&cfg, floor_kernel, status);
+}
+
+cudaError_t floor_work_launch(const Params& p, const Launch& l, int work, cudaStream_t s) {
+    using K = void (*)(const Params, const int, const int);
+    K k = l.cpt == 1 ? floor_work_kernel<1> : l.cpt == 2 ? floor_work_kernel<2> : l.cpt == 4 ? floor_work_kernel<4>
+                                                                                            : nullptr;
+    if (!k) return cudaErrorInvalidValue;
+    if (l.cluster > 8) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attrs[2];
+    fill_config(cfg, attrs, l, s);
+    return cudaLaunchKernelEx(&cfg, k, p, l.cluster, work | (l.prefetch_out ? kFloorPrefetchOut : 0));
 }
 
 bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt, true, false, true) != nullptr; }
