@@ -563,8 +563,9 @@ def decode_against_floor(mfr, device, wl, args, replays=25, ncalls=4096):
 def bandwidth_row(mfr, device, wl, args, steps, peak, repeat_check=False):
     """µs/call, GB/s and fraction of the measured copy bandwidth for one
     workload, timed like the headline step (CUDA events around `steps`
-    calls on one stream; input/output sets rotate so that together they
-    exceed 3x L2 and no call starts with its data in L2).  With
+    calls on one stream, captured in a CUDA graph and replayed three times
+    when a call moves less than 256 MB; input/output sets rotate so that
+    together they exceed 3x L2 and no call starts with its data in L2).  With
     repeat_check, two further calls into fresh buffers must reproduce the
     first call's outputs bit for bit."""
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -591,15 +592,32 @@ def bandwidth_row(mfr, device, wl, args, steps, peak, repeat_check=False):
     for i in range(max(3, nsets)):
         step(i)
     stream.synchronize()
+    # calls shorter than a Python launch go through a CUDA graph, so the host
+    # does not set the pace; larger calls are launched one by one
+    graph = None
+    if nbytes < (256 << 20):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(steps):
+                    step(i)
+            graph.replay()
+        stream.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(device.index) as clocks:
+    reps = 3 if graph is not None else 1
+    with ClockSampler(device.index) as clocks, torch.cuda.stream(stream):
         clocks.wait_first()
         a.record(stream)
-        for i in range(steps):
-            step(i)
+        for _ in range(reps):
+            if graph is not None:
+                graph.replay()     # on the current stream, which is `stream` here
+            else:
+                for i in range(steps):
+                    step(i)
         b.record(stream)
         b.synchronize()
-    us = a.elapsed_time(b) * 1e3 / steps
+    us = a.elapsed_time(b) * 1e3 / (steps * reps)
+    del graph
     info = plan.info()
     row = {"workload": wl.name, "T": T, "H": H, "us_per_call": round(us, 2),
            "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1), "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4),
