@@ -120,6 +120,13 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
         // 6 % faster from one lane (246 vs 263 us, its writes compete with a
         // faster read stream), and the NVFP4 form 1.4 % faster in parallel.
         constexpr bool kParallelIssue = !FUSED || FP4;
+        // The residual + bf16 form with four or more tiles per token (H > 4096)
+        // issues the first two fills of its ring from the slots' own lanes and
+        // the rest from one lane.  Measured on two GB300s against one-lane
+        // issue throughout: H = 8192 at T = 1024 / 4096 / 8192 / 32768 1.8 /
+        // 2.3 / 2.7 / 2.1 % faster, T = 512 unchanged; at H = 4096 (two tiles)
+        // the same change made prefill 1.3 % slower, so those stay one-lane.
+        constexpr int64_t kParallelFills = (FUSED && !FP4 && MAXTILES >= 4) ? 2 : 0;
         // No explicit launch_dependents: every CTA of this persistent grid runs
         // from start to end, so an early signal would let a dependent grid park
         // its CTAs on every SM for the whole call (measured: a following
@@ -175,7 +182,7 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask) * cb * 2 + (FUSED ? cb * 4 : 0)));
                 }
                 __syncwarp();
-                if constexpr (kParallelIssue) {
+                if (kParallelIssue || fill < kParallelFills) {
                     if (valid)
                         bulk_g2s(smem_u32(st + kHeaderBytes + lane * row_bytes),
                                  p.expert_out + static_cast<int64_t>(row) * H + c0, static_cast<uint32_t>(cb * 2), bar);
