@@ -77,6 +77,9 @@ def parse_args(argv=None):
     ap.add_argument("--variant", default="auto", choices=["auto", "rows", "stream", "cluster"])
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T of the workload (small cases for profiling)")
+    ap.add_argument("--floor-probe", type=int, default=None, metavar="T",
+                    help=argparse.SUPPRESS)   # internal: the launch floor of decode T in a fresh process
+    ap.add_argument("--floor-device", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -460,34 +463,94 @@ def _quartiles(xs):
     return float(q[1]), float(q[2] - q[0])
 
 
-def decode_against_floor(mfr, device, wl, args, replays=25, ncalls=4096):
+FLOOR_CALLS = 4096
+
+
+def floor_graph_times(mfr, device, plan, replays, ncalls=FLOOR_CALLS):
+    """Per-launch µs of `replays` replays of a CUDA graph of `ncalls` empty
+    kernels with the plan's launch geometry (two untimed replays first)."""
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(ncalls):
+                plan.launch_floor(stream)
+        for _ in range(3):
+            graph.replay()
+        stream.synchronize()
+        times = []
+        for _ in range(replays):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3 / ncalls)
+    del graph
+    return times
+
+
+def run_floor_probe(args):
+    """--floor-probe T: the launch floor of the decode plan for T tokens,
+    measured in this fresh process before any other work (printed as one
+    JSON line)."""
+    import moe_finalize_residual_rmsnorm_gb300 as mfr
+    torch.cuda.set_device(args.floor_device)
+    device = torch.device("cuda", args.floor_device)
+    mfr.load_library()
+    wl = W.decode(args.floor_probe)
+    plan = mfr.Plan(wl.T, wl.H, wl.k, wl.R, enable_pdl=not args.no_pdl)
+    times = floor_graph_times(mfr, device, plan, 25)
+    med, iqr = _quartiles(times)
+    print(json.dumps({"T": wl.T, "floor_us": med, "floor_iqr": iqr, "replays": len(times)}), flush=True)
+
+
+def fresh_process_floors(device, tokens, args):
+    """The launch floor of each decode size, each in a fresh process of its
+    own.  An empty kernel's launch rate depends on the state of the process:
+    in a fresh one a graph of 4096 empty 4-CTA launches runs 0.35 us per
+    launch, and after other graphs of thousands of launches (even destroyed
+    ones) or large calls have run in it, 0.53-0.59 us, on the same GPU
+    (measured).  The fresh figure is the lower and the reproducible one, so
+    it is the floor the decode target is computed on."""
+    floors = {}
+    for T in tokens:
+        cmd = [sys.executable, os.path.abspath(__file__), "--floor-probe", str(T), "--floor-device", str(device.index)]
+        if args.no_pdl:
+            cmd.append("--no-pdl")
+        out = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+        if out.returncode != 0:
+            raise RuntimeError(f"floor probe for T={T} failed: {out.stderr[-500:]}")
+        floors[T] = json.loads(out.stdout.strip().splitlines()[-1])
+    return floors
+
+
+def decode_against_floor(mfr, device, wl, args, replays=25, ncalls=4096, floor=None):
     """One decode size: the call, its launch floor and its one-pass floors,
     measured in the same run.
 
     Every figure is a CUDA graph of `ncalls` launches on one stream, per
-    launch.  The call graph cycles through enough input/output sets to
-    exceed 3x L2, so each call reads cold data.  The floor graphs use the
-    plan's exact launch geometry and PDL attribute:
-      floor_us             the empty kernel (moe_finalize_rmsnorm_launch_floor),
-                           timed on the second of two back-to-back replays: the
-                           launch path in its steady state (the launch floor
-                           the decode target is defined on)
-      floor_after_call_us  the first of those two replays, right after a call
-                           replay: launches of a graph that follows data-moving
-                           work run slower (context)
-      load_floor_us, store_floor_us  the empty kernel plus only the call's
-                           loads (LOAD), or only its stores (STORE)
-      pass_floor_us        the empty kernel plus the call's loads and stores
-                           over the same cold input sets, no arithmetic
-                           (moe_finalize_rmsnorm_launch_floor_work, LOAD|STORE):
-                           launch plus one pass over the call's bytes, measured
-      pass_exchange_floor_us  the same with one cluster barrier between loads
-                           and stores (LOAD|EXCHANGE|STORE)
-    One round replays call, floor, floor, load, store, pass, pass + exchange; `replays`
-    rounds; median and interquartile range of each; the SM clock is sampled
-    meanwhile.  The target is us_per_call <= 2 * (floor_us + bytes / 8 TB/s)
-    (vs_2x_floor, same-run medians); vs_2x_pass_floor compares with twice the
-    measured one-pass floor instead."""
+    launch, median and interquartile range over `replays` replays.  All use
+    the plan's exact launch geometry and PDL attribute.
+      floor_us     the empty kernel (moe_finalize_rmsnorm_launch_floor), the
+                   launch floor the decode target is defined on, measured in a
+                   fresh process (`floor`, from fresh_process_floors) when
+                   given; floor_in_process_us is the same graph measured here,
+                   alone and after two untimed replays (the first replay of an
+                   empty-kernel graph after data-moving work runs up to 2.5x
+                   slower), as context.
+      us_per_call  the call, cycling through enough input/output sets to
+                   exceed 3x L2 (each call reads cold data).
+      load_floor_us, store_floor_us, pass_floor_us, pass_exchange_floor_us
+                   the empty kernel plus only the call's loads, only its
+                   stores, both, and both with one cluster barrier between
+                   them, over the same cold input sets, no arithmetic
+                   (moe_finalize_rmsnorm_launch_floor_work): the launch plus
+                   one pass over the call's bytes, measured.
+    The call and the four work floors are replayed in turn, `replays`
+    rounds.  The SM clock is sampled throughout.  The target is
+    us_per_call <= 2 * (floor_us + bytes / 8 TB/s) (vs_2x_floor);
+    vs_2x_pass_floor compares with twice the measured one-pass floor."""
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     nbytes = W.algorithmic_bytes(wl.T, wl.H, wl.k)
     nsets = int(min(ncalls, max(2, -(-3 * l2 // max(nbytes, 1)))))
@@ -504,53 +567,58 @@ def decode_against_floor(mfr, device, wl, args, replays=25, ncalls=4096):
     stream = torch.cuda.Stream(device)
     work = {"load": mfr.FLOOR_LOAD, "store": mfr.FLOOR_STORE, "pass": mfr.FLOOR_LOAD | mfr.FLOOR_STORE,
             "pass_exchange": mfr.FLOOR_LOAD | mfr.FLOOR_EXCHANGE | mfr.FLOOR_STORE}
-    graphs = {}
-    with torch.cuda.stream(stream):
-        for kind in ("call", "floor", "load", "store", "pass", "pass_exchange"):
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                for i in range(ncalls):
-                    j = i % nsets
-                    if kind == "floor":
-                        plan.launch_floor(stream)
-                    elif kind == "call":
-                        plan.run(E[j], idx[j], w[j], res[j], rout[j], g, eps, out[j], stream, validate=False)
-                    else:
-                        plan.launch_floor_work(work[kind], E[j], idx[j], res[j], rout[j], out[j], stream)
-            graph.replay()
-            graphs[kind] = graph
+
+    def capture(kind):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(ncalls):
+                j = i % nsets
+                if kind == "floor":
+                    plan.launch_floor(stream)
+                elif kind == "call":
+                    plan.run(E[j], idx[j], w[j], res[j], rout[j], g, eps, out[j], stream, validate=False)
+                else:
+                    plan.launch_floor_work(work[kind], E[j], idx[j], res[j], rout[j], out[j], stream)
+        graph.replay()
         stream.synchronize()
+        return graph
 
-        def timed(kind):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            graphs[kind].replay()
-            b.record(stream)
-            b.synchronize()
-            return a.elapsed_time(b) * 1e3 / ncalls
+    def timed(graph):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) * 1e3 / ncalls
 
-        times = {"call": [], "floor_after_call": [], "floor": [], "load": [], "store": [], "pass": [],
-                 "pass_exchange": []}
-        with ClockSampler(device.index) as clocks:
-            clocks.wait_first()
-            for _ in range(replays):
-                times["call"].append(timed("call"))
-                times["floor_after_call"].append(timed("floor"))
-                times["floor"].append(timed("floor"))
-                for kind in ("load", "store", "pass", "pass_exchange"):
-                    times[kind].append(timed(kind))
+    times = {kind: [] for kind in ("floor", "call", *work)}
+    with ClockSampler(device.index) as clocks, torch.cuda.stream(stream):
+        clocks.wait_first()
+        floor_graph = capture("floor")
+        for _ in range(2):
+            timed(floor_graph)
+        times["floor"] = [timed(floor_graph) for _ in range(replays)]
+        del floor_graph
+        graphs = {kind: capture(kind) for kind in ("call", *work)}
+        for _ in range(replays):
+            for kind, graph in graphs.items():
+                times[kind].append(timed(graph))
+        del graphs
     if plan.get_status(stream) != 0:
         raise RuntimeError(f"the device status word reported an error during {wl.name}")
     q = {kind: _quartiles(v) for kind, v in times.items()}
-    us, fl, ps = q["call"][0], q["floor"][0], q["pass"][0]
+    us, ps = q["call"][0], q["pass"][0]
+    fl_here, fl_here_iqr = q["floor"]
+    fl, fl_iqr = (floor["floor_us"], floor["floor_iqr"]) if floor else (fl_here, fl_here_iqr)
     ck = clocks.summary()
     info = plan.info()
-    del graphs, E, idx, w, res, rout, out, base
+    del E, idx, w, res, rout, out, base
     torch.cuda.empty_cache()
     return {"workload": wl.name, "T": T, "H": H, "us_per_call": round(us, 3), "us_iqr": round(q["call"][1], 3),
-            "floor_us": round(fl, 3), "floor_iqr": round(q["floor"][1], 3),
+            "floor_us": round(fl, 3), "floor_iqr": round(fl_iqr, 3),
+            "floor_where": "fresh process" if floor else "this process",
             "vs_2x_floor": round(us / (2 * (fl + nbytes / 8e12 * 1e6)), 3),
-            "floor_after_call_us": round(q["floor_after_call"][0], 3),
+            "floor_in_process_us": round(fl_here, 3),
             "load_floor_us": round(q["load"][0], 3), "store_floor_us": round(q["store"][0], 3),
             "pass_floor_us": round(ps, 3), "pass_floor_iqr": round(q["pass"][1], 3),
             "pass_exchange_floor_us": round(q["pass_exchange"][0], 3),
@@ -652,7 +720,8 @@ def run_compact_sweep(mfr, device, args):
     bitwise-repeat check (bandwidth_row)."""
     peak, _ = measured_peak()
     t0 = time.perf_counter()
-    decode = [decode_against_floor(mfr, device, W.decode(t), args) for t in (1, 2, 4, 8)]
+    floors = fresh_process_floors(device, (1, 2, 4, 8), args)
+    decode = [decode_against_floor(mfr, device, W.decode(t), args, floor=floors[t]) for t in (1, 2, 4, 8)]
     bandwidth = [bandwidth_row(mfr, device, W.wide(512), args, 400, peak),
                  bandwidth_row(mfr, device, W.wide(4096), args, 60, peak),
                  bandwidth_row(mfr, device, W.wide(8192), args, 40, peak),
@@ -956,7 +1025,9 @@ def main(argv=None):
     if args.warmup < 3:
         print("bench.py: --warmup must be >= 3", file=sys.stderr)
         return 2
-    if args.impl == "reference":
+    if args.floor_probe is not None:
+        run_floor_probe(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         if not torch.cuda.is_available():
