@@ -16,7 +16,8 @@ import torch
 
 import moe_finalize_residual_rmsnorm_gb300 as mfr
 import workloads as W
-from helpers import bf16_bits, bf16_ulp_distance, oracle_expert_norm
+import oracle
+from helpers import bf16_bits, bf16_ulp_distance, host_inputs, oracle_expert_norm, over_all_tokens
 
 pytestmark = pytest.mark.gpu
 GUARD = 256
@@ -143,18 +144,26 @@ def test_expert_norm_bad_and_sentinel_slots(variant):
 
 
 @pytest.mark.parametrize("wl", [W.PREFILL, W.wide(4096)], ids=["prefill", "wide_T4096"])
-def test_expert_norm_full_size_sampled(wl):
+def test_expert_norm_full_size_every_token(wl):
     """Full-size workloads in the launch configuration the benchmark times
-    (the ring form); sampled tokens against the oracle."""
+    (the ring form); every token against the oracle, run over the host
+    cores."""
     inp = W.make_inputs(wl, "cuda")
     got, plan = run_expert_norm(inp)
     assert plan.info()["variant"] == mfr.VARIANT_STREAM
-    rng = np.random.default_rng(5)
-    tokens = np.sort(rng.choice(wl.T, size=48, replace=False))
-    tokens[0], tokens[-1] = 0, wl.T - 1
-    want, y, s, _ = oracle_expert_norm(inp, tokens=tokens)
-    assert_expert_norm_close(got[tokens], want, y, s)
     assert plan.get_status() == 0
+    h = host_inputs(inp)
+    del inp
+    torch.cuda.empty_cache()
+    E_abs, w_abs, g_abs = h["E"] & np.uint16(0x7FFF), np.abs(h["w"]), h["gamma"] & np.uint16(0x7FFF)
+
+    def check(tk):
+        want, bad = oracle.finalize_expert_rmsnorm(h["E"], h["idx"], h["w"], h["gamma"], h["eps"], tokens=tk)
+        assert bad == 0
+        y, _ = oracle.expert_rmsnorm_f64(h["E"], h["idx"], h["w"], h["gamma"], h["eps"], tokens=tk)
+        sc, _ = oracle.expert_rmsnorm_f64(E_abs, h["idx"], w_abs, g_abs, h["eps"], tokens=tk)
+        assert_expert_norm_close(got[tk[0]:tk[-1] + 1], want, y, sc)
+    assert over_all_tokens(wl.T, check) == wl.T
 
 
 def test_expert_norm_refuses_other_variants_and_other_plans():
