@@ -402,7 +402,8 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "e2e": e2e,
     }
-    if not args.no_sweep and not args.tokens:
+    if rank == 0 and not args.no_sweep and not args.tokens:
+        # per-GPU figures of the metric's other sizes: rank 0 alone measures them
         result["sweep"] = run_compact_sweep(mfr, device, args)
     if args.sweep:
         result["sweep_full"] = run_sweep(mfr, device, args)
