@@ -416,6 +416,7 @@ def run_ours(args):
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:
+        barrier(dist, device)      # the other ranks wait for rank 0's sweep and CPU baseline
         dist.destroy_process_group()
 
 
