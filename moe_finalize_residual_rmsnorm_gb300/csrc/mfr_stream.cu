@@ -182,7 +182,7 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask) * cb * 2 + (FUSED ? cb * 4 : 0)));
                 }
                 __syncwarp();
-                if (kParallelIssue || fill < kParallelFills) {
+                if (kParallelIssue || (kParallelFills > 0 && fill < kParallelFills)) {
                     if (valid)
                         bulk_g2s(smem_u32(st + kHeaderBytes + lane * row_bytes),
                                  p.expert_out + static_cast<int64_t>(row) * H + c0, static_cast<uint32_t>(cb * 2), bar);
