@@ -520,10 +520,16 @@ def fresh_process_floors(device, tokens, args):
         cmd = [sys.executable, os.path.abspath(__file__), "--floor-probe", str(T), "--floor-device", str(device.index)]
         if args.no_pdl:
             cmd.append("--no-pdl")
-        out = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
-        if out.returncode != 0:
-            raise RuntimeError(f"floor probe for T={T} failed: {out.stderr[-500:]}")
-        floors[T] = json.loads(out.stdout.strip().splitlines()[-1])
+        try:
+            out = subprocess.run(cmd, capture_output=True, text=True, timeout=300)
+            if out.returncode == 0:
+                floors[T] = json.loads(out.stdout.strip().splitlines()[-1])
+                continue
+            why = out.stderr.strip().splitlines()[-1:] or [f"exit code {out.returncode}"]
+        except (subprocess.TimeoutExpired, OSError, ValueError, IndexError) as e:
+            why = [repr(e)]
+        # the row then falls back to the floor measured in this process, and says so
+        print(f"bench.py: fresh-process floor for T={T} not measured: {why[0][:200]}", file=sys.stderr)
     return floors
 
 
@@ -723,7 +729,7 @@ def run_compact_sweep(mfr, device, args):
     peak, _ = measured_peak()
     t0 = time.perf_counter()
     floors = fresh_process_floors(device, (1, 2, 4, 8), args)
-    decode = [decode_against_floor(mfr, device, W.decode(t), args, floor=floors[t]) for t in (1, 2, 4, 8)]
+    decode = [decode_against_floor(mfr, device, W.decode(t), args, floor=floors.get(t)) for t in (1, 2, 4, 8)]
     bandwidth = [bandwidth_row(mfr, device, W.wide(512), args, 400, peak),
                  bandwidth_row(mfr, device, W.wide(4096), args, 60, peak),
                  bandwidth_row(mfr, device, W.wide(8192), args, 40, peak),
