@@ -98,6 +98,8 @@ class Oracle:
         lib.mfr_oracle_nvfp4_quantize.restype = None
         lib.mfr_oracle_nvfp4_encode.argtypes = [i64, i64, p, ctypes.c_float, p, p]
         lib.mfr_oracle_nvfp4_encode.restype = None
+        lib.mfr_oracle_nvfp4_swizzle_scales.argtypes = [i64, i64, p, p]
+        lib.mfr_oracle_nvfp4_swizzle_scales.restype = None
         lib.mfr_oracle_finalize_residual_rmsnorm_nvfp4.argtypes = [
             i64, i64, i64, i64, p, p, p, p, p, ctypes.c_float, ctypes.c_float, p, p, p, p, i64, p, p]
         lib.mfr_oracle_finalize_residual_rmsnorm_nvfp4.restype = i64
@@ -276,6 +278,15 @@ class Oracle:
         self.lib.mfr_oracle_nvfp4_encode(n, H, _ptr(y), ctypes.c_float(s_enc), _ptr(sf), _ptr(q))
         return q
 
+    def nvfp4_swizzle_scales(self, sf, fill: int = 0):
+        """Block scales uint8 [n, S] -> the tiled layout block-scaled GEMMs
+        read: uint8 [ceil(n/128)*128 * ceil(S/4)*4], padding bytes = fill."""
+        sf = _c(sf, np.uint8)
+        n, S = sf.shape
+        out = np.full(-(-n // 128) * 128 * (-(-S // 4) * 4), fill, dtype=np.uint8)
+        self.lib.mfr_oracle_nvfp4_swizzle_scales(n, S, _ptr(sf), _ptr(out))
+        return out
+
     def finalize_residual_rmsnorm_nvfp4(self, expert_out_bits, permuted_row_of, topk_weights, residual_in,
                                         gamma_bits, eps: float, s_enc: float,
                                         tokens: Optional[Sequence[int]] = None):
@@ -348,6 +359,10 @@ def nvfp4_quantize(*a, **kw):
 
 def nvfp4_encode(*a, **kw):
     return default().nvfp4_encode(*a, **kw)
+
+
+def nvfp4_swizzle_scales(*a, **kw):
+    return default().nvfp4_swizzle_scales(*a, **kw)
 
 
 def finalize_residual_rmsnorm_nvfp4(*a, **kw):

@@ -436,6 +436,25 @@ void mfr_oracle_nvfp4_encode(int64_t n, int64_t H, const float* y, float s_enc,
                                s_enc, q_packed + i * (H / 2) + b * 8);
 }
 
+/* The block scales of n rows (S scale bytes per row, one per 16 columns) in
+ * the tiled layout that block-scaled FP4 GEMMs read, from the public
+ * description of the 1-D block-scaling-factor layout: the scale matrix,
+ * padded to a multiple of 128 rows and of 4 columns, is cut into tiles of
+ * 128 rows x 4 columns, each stored as 512 consecutive bytes, tiles in
+ * row-major order of (row / 128, column / 4); inside a tile, scale (r, c)
+ * sits at byte (r mod 32) * 16 + ((r / 32) mod 4) * 4 + (c mod 4).  Bytes of
+ * the padding are not written. */
+void mfr_oracle_nvfp4_swizzle_scales(int64_t n, int64_t S, const uint8_t* sf, uint8_t* out)
+{
+    int64_t col_tiles = (S + 3) / 4;
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t c = 0; c < S; ++c) {
+            int64_t tile = (r / 128) * col_tiles + c / 4;
+            int64_t within = (r % 32) * 16 + ((r / 32) % 4) * 4 + (c % 4);
+            out[tile * 512 + within] = sf[r * S + c];
+        }
+}
+
 /* The whole path with the NVFP4 epilogue: the residual as above, RMSNorm in
  * double, the normalised value rounded once to FP32 (the precision the
  * quantiser works in), then quantised. */

@@ -72,6 +72,12 @@ MUTATIONS = {
     "encode_ignores_the_given_scale": [
         ("nvfp4_encode_block(y + i * H + b * 16, (float)mfr_oracle_e4m3_to_f64(sf[i * (H / 16) + b]),",
          "nvfp4_encode_block(y + i * H + b * 16, 1.0f,")],
+    "scale_tiles_without_the_row_group": [
+        ("int64_t within = (r % 32) * 16 + ((r / 32) % 4) * 4 + (c % 4);",
+         "int64_t within = (r % 32) * 16 + (c % 4);")],
+    "scale_tiles_column_major": [
+        ("int64_t tile = (r / 128) * col_tiles + c / 4;",
+         "int64_t tile = (c / 4) * ((n + 127) / 128) + r / 128;")],
     "amax_over_8": [("            for (int j = 0; j < 16; ++j)\n                if (fabsf(yb[j]) > amax)",
                      "            for (int j = 0; j < 8; ++j)\n                if (fabsf(yb[j]) > amax)")],
     "expert_norm_gamma_dropped": [

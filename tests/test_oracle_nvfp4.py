@@ -127,3 +127,37 @@ def test_encode_at_the_quantisers_own_scales_gives_its_codes(oracle_lib):
     mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
     best = np.min(np.abs(np.abs(z)[..., None] - mags), axis=-1)
     assert np.all(np.abs(oracle_lib.e2m1_to_f64(codes) - z) <= best + 1e-12)
+
+
+def test_hand_worked_scale_tile_offsets(oracle_lib):
+    """The tiled block-scale layout of block-scaled FP4 GEMMs, by hand."""
+    with open(os.path.join(GOLDEN, "nvfp4_scale_tiles_hand_worked.json")) as f:
+        g = json.load(f)
+    n, S = g["n"], g["S"]
+    # every scale carries its own (row, col) code, so its position can be found
+    sf = np.zeros((n, S), dtype=np.uint8)
+    for case in g["cases"]:
+        sf[case["row"], case["col"]] = 1 + g["cases"].index(case)
+    out = oracle_lib.nvfp4_swizzle_scales(sf, fill=0)
+    assert out.size == g["total_bytes"]
+    for i, case in enumerate(g["cases"]):
+        assert np.flatnonzero(out == i + 1).tolist() == [case["offset"]], case
+
+
+def test_scale_tiles_are_a_bijection_and_leave_padding(oracle_lib):
+    """Full tiles: every byte receives exactly one scale.  Partial tiles: the
+    padding keeps its fill byte, nothing else does."""
+    n, S = 256, 8
+    idx = np.arange(n * S, dtype=np.int64)
+    lo = (idx & 0xFF).astype(np.uint8).reshape(n, S)
+    hi = (idx >> 8).astype(np.uint8).reshape(n, S)
+    back = oracle_lib.nvfp4_swizzle_scales(lo).astype(np.int64) | \
+        (oracle_lib.nvfp4_swizzle_scales(hi).astype(np.int64) << 8)
+    assert sorted(back.tolist()) == list(range(n * S))
+    sf = np.full((5, 3), 7, dtype=np.uint8)
+    out = oracle_lib.nvfp4_swizzle_scales(sf, fill=0xEE)
+    assert out.size == 128 * 4 and (out == 7).sum() == 15 and (out == 0xEE).sum() == 128 * 4 - 15
+    # rows 32 apart share a 16-byte group; consecutive rows are 16 bytes apart
+    pos = {v: int(np.flatnonzero(oracle_lib.nvfp4_swizzle_scales(
+        np.where(np.arange(128)[:, None] == v, 9, 0).astype(np.uint8)[:, :4]) == 9)[0]) for v in (0, 1, 32, 64, 96)}
+    assert pos == {0: 0, 1: 16, 32: 4, 64: 8, 96: 12}
