@@ -895,7 +895,8 @@ def run_variants(mfr, device, wl, sets, args):
     like the main step (two alternating input sets, CUDA events):
     plain finalize (bf16 sum, no residual or norm: k*H*2 + H*2 + k*8 bytes
     per token), the NVFP4 epilogue (residual + RMSNorm, output as E2M1
-    codes + E4M3 block scales: k*H*2 + H*8 + H/2 + H/16 + k*8 bytes) and the
+    codes + E4M3 block scales: k*H*2 + H*8 + H/2 + H/16 + k*8 bytes), the
+    same with the scales in the tiled layout of block-scaled GEMMs, and the
     finalize with an RMSNorm per expert row (k*H*2 + H*2 + k*8 bytes)."""
     T, H, k, R = wl.T, wl.H, wl.k, wl.R
     steps = max(20, min(args.steps, 500))
@@ -903,9 +904,11 @@ def run_variants(mfr, device, wl, sets, args):
     out = {}
     fin = mfr.FinalizePlan(T, H, k, R, enable_pdl=not args.no_pdl)
     fp4 = mfr.Nvfp4Plan(T, H, k, R, enable_pdl=not args.no_pdl)
+    fp4t = mfr.Nvfp4Plan(T, H, k, R, enable_pdl=not args.no_pdl, sf_layout=mfr.SF_TILED_128x4)
     en = mfr.ExpertNormPlan(T, H, k, R, enable_pdl=not args.no_pdl)
     q = [torch.empty((T, H // 2), dtype=torch.uint8, device=device) for _ in range(2)]
     sf = [torch.empty((T, H // 16), dtype=torch.uint8, device=device) for _ in range(2)]
+    sft = [torch.empty((fp4t.sf_bytes(),), dtype=torch.uint8, device=device) for _ in range(2)]
     s_enc = 448.0 * 6.0 / 16.0
 
     def fin_step(i):
@@ -917,14 +920,21 @@ def run_variants(mfr, device, wl, sets, args):
         fp4.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["residual"], d["residual_out"],
                 d["gamma"], d["eps"], s_enc, q[i & 1], sf[i & 1], stream, validate=False)
 
+    def fp4t_step(i):
+        d = sets[i & 1]
+        fp4t.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["residual"], d["residual_out"],
+                 d["gamma"], d["eps"], s_enc, q[i & 1], sft[i & 1], stream, validate=False)
+
     def en_step(i):
         d = sets[i & 1]
         en.run(d["expert_out"], d["permuted_row_of"], d["topk_weights"], d["gamma"], d["eps"], d["out"], stream,
                validate=False)
 
-    plans = {"finalize_only": fin, "nvfp4_epilogue": fp4, "expert_rmsnorm": en}
+    plans = {"finalize_only": fin, "nvfp4_epilogue": fp4, "nvfp4_epilogue_tiled_scales": fp4t, "expert_rmsnorm": en}
     for name, fn, nbytes in (("finalize_only", fin_step, T * (k * H * 2 + H * 2 + k * 8)),
                              ("nvfp4_epilogue", fp4_step, T * (k * H * 2 + H * 8 + H // 2 + H // 16 + k * 8)),
+                             ("nvfp4_epilogue_tiled_scales", fp4t_step,
+                              T * (k * H * 2 + H * 8 + H // 2 + H // 16 + k * 8)),
                              ("expert_rmsnorm", en_step, T * (k * H * 2 + H * 2 + k * 8))):
         for i in range(5):
             fn(i)
@@ -939,7 +949,7 @@ def run_variants(mfr, device, wl, sets, args):
         out[name] = {"us_per_call": round(us, 2), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                      "bytes_per_call": int(nbytes), "steps": steps,
                      "variant": plans[name].info()["variant_name"]}
-    if fin.get_status(stream) or fp4.get_status(stream) or en.get_status(stream):
+    if fin.get_status(stream) or fp4.get_status(stream) or fp4t.get_status(stream) or en.get_status(stream):
         raise RuntimeError("status word set while timing the variants")
     return out
 

@@ -167,14 +167,40 @@ int moe_finalize_rmsnorm_run(mfr_plan_t plan,
  *          448 * 6 / amax over the tensor, measured offline
  *  out_q   device, uint8 [T, H/2], 4-byte aligned: two codes per byte,
  *          column 2j in the low nibble of byte j
- *  out_sf  device, uint8 [T, H/16]: E4M3 block scales, row-major (not the
- *          swizzled layout some GEMMs read)
+ *  out_sf  device, uint8: E4M3 block scales, [T, H/16] row-major, or for
+ *          plans made with MFR_SF_TILED_128x4 the tiled layout below
  * residual_out is written as in moe_finalize_rmsnorm_run.  Needs H % 16 == 0.
  * Plans come from moe_finalize_rmsnorm_nvfp4_plan (same arguments and
  * options as moe_finalize_rmsnorm_plan) and run only with
  * moe_finalize_rmsnorm_nvfp4_run. */
 int moe_finalize_rmsnorm_nvfp4_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
                                     const mfr_options* opt);
+
+/* The same plan with a choice of block-scale layout for out_sf:
+ *  MFR_SF_ROW_MAJOR    uint8 [T, H/16], row-major (moe_finalize_rmsnorm_nvfp4_plan)
+ *  MFR_SF_TILED_128x4  the layout block-scaled FP4 GEMMs read for their
+ *                      operand scales (the public 1-D block-scaling-factor
+ *                      layout): the [T, H/16] scale matrix, padded to a
+ *                      multiple of 128 rows and of 4 columns, is cut into
+ *                      tiles of 128 rows x 4 columns stored as 512 consecutive
+ *                      bytes each, tiles in row-major order of (row / 128,
+ *                      column / 4); scale (r, c) sits at byte
+ *                      (r mod 32) * 16 + ((r / 32) mod 4) * 4 + (c mod 4) of its
+ *                      tile.  out_sf then holds ceil(T/128)*128 x
+ *                      ceil(H/64)*4 bytes; the padding bytes are not written
+ *                      (a GEMM that reads padded rows or columns needs them,
+ *                      and the matching rows / columns of out_q, set by the
+ *                      caller).  out_q is [T, H/2] as before.
+ * Any other sf_layout is MFR_ERR_INVALID_ARG.  moe_finalize_rmsnorm_nvfp4_run
+ * runs both kinds. */
+#define MFR_SF_ROW_MAJOR   0
+#define MFR_SF_TILED_128x4 1
+int moe_finalize_rmsnorm_nvfp4_plan_ex(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                                       const mfr_options* opt, int sf_layout);
+
+/* Bytes of out_sf for an NVFP4 plan in its layout (T * H/16 row-major); -1
+ * for a NULL or non-NVFP4 plan. */
+int64_t moe_finalize_rmsnorm_nvfp4_sf_bytes(mfr_plan_t plan);
 int moe_finalize_rmsnorm_nvfp4_run(mfr_plan_t plan, const void* expert_out,
                                    const int32_t* permuted_row_of, const float* topk_weights,
                                    const float* residual_in, float* residual_out, const void* gamma,

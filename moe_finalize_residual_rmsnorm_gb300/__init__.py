@@ -22,7 +22,7 @@ from .build import LIBRARY, build as _build_library
 __all__ = [
     "LIBRARY", "MFRError", "Plan", "FinalizePlan", "Nvfp4Plan", "ExpertNormPlan", "PlanInfo", "Options", "build", "load_library", "supports",
     "moe_finalize_residual_rmsnorm", "finalize_residual_rmsnorm_host", "exported_symbols",
-    "run_noalloc", "validate_fused_args", "VARIANT_AUTO", "VARIANT_CLUSTER", "VARIANT_ROWS", "VARIANT_STREAM", "STATUS_BAD_INDEX",
+    "run_noalloc", "validate_fused_args", "SF_ROW_MAJOR", "SF_TILED_128x4", "VARIANT_AUTO", "VARIANT_CLUSTER", "VARIANT_ROWS", "VARIANT_STREAM", "STATUS_BAD_INDEX",
     "ERROR_CODES",
 ]
 
@@ -33,6 +33,7 @@ ERROR_CODES = {
 }
 STATUS_BAD_INDEX = 1
 STATUS_TIMEOUT = 2
+SF_ROW_MAJOR, SF_TILED_128x4 = 0, 1
 FLOOR_LOAD, FLOOR_EXCHANGE, FLOOR_STORE = 1, 2, 4
 VARIANT_AUTO, VARIANT_CLUSTER, VARIANT_ROWS, VARIANT_STREAM = 0, 1, 2, 3
 VARIANT_NAMES = {VARIANT_CLUSTER: "cluster", VARIANT_ROWS: "rows", VARIANT_STREAM: "stream"}
@@ -79,6 +80,9 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_run_host": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _F, _VP, _VP, _I64, _VP]),
     "moe_finalize_rmsnorm_nvfp4_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
     "moe_finalize_rmsnorm_nvfp4_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _F, _F, _VP, _VP, _VP]),
+    "moe_finalize_rmsnorm_nvfp4_plan_ex": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options),
+                                                 _I]),
+    "moe_finalize_rmsnorm_nvfp4_sf_bytes": (_I64, [_VP]),
     "moe_finalize_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
     "moe_finalize_run": (_I, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "moe_finalize_expert_rmsnorm_plan": (_I, [ctypes.POINTER(_VP), _I64, _I64, _I, _I64, ctypes.POINTER(Options)]),
@@ -295,12 +299,34 @@ class Plan:
 
 class Nvfp4Plan(Plan):
     """Residual + RMSNorm with the normalised output written as NVFP4
-    (C: moe_finalize_rmsnorm_nvfp4_plan / moe_finalize_rmsnorm_nvfp4_run):
+    (C: moe_finalize_rmsnorm_nvfp4_plan_ex / moe_finalize_rmsnorm_nvfp4_run):
     out_q uint8 [T, H/2] (two E2M1 codes per byte, even column in the low
-    nibble), out_sf uint8 [T, H/16] (E4M3 block scales), s_enc the FP32
-    tensor scale."""
+    nibble), out_sf the E4M3 block scales, uint8 [T, H/16] row-major
+    (sf_layout=SF_ROW_MAJOR) or sf_bytes() bytes in the 128 x 4 tiles that
+    block-scaled FP4 GEMMs read (SF_TILED_128x4); s_enc the FP32 tensor
+    scale."""
 
     _PLAN_FN = "moe_finalize_rmsnorm_nvfp4_plan"
+
+    def __init__(self, T: int, H: int, k: int, R: Optional[int] = None, *, sf_layout: int = SF_ROW_MAJOR,
+                 enable_pdl: bool = True, variant: int = VARIANT_AUTO, cluster_size: int = 0,
+                 debug_checks: bool = False, sentinel_skip: bool = False):
+        lib = load_library()
+        self._lib = lib
+        self.T, self.H, self.k = int(T), int(H), int(k)
+        self.R = int(T) * int(k) if R is None else int(R)
+        self.sf_layout = int(sf_layout)
+        opt = Options(int(bool(enable_pdl)), int(variant), int(cluster_size), int(bool(debug_checks)),
+                      int(bool(sentinel_skip)))
+        h = ctypes.c_void_p()
+        _check(lib.moe_finalize_rmsnorm_nvfp4_plan_ex(ctypes.byref(h), self.T, self.H, self.k, self.R,
+                                                      ctypes.byref(opt), self.sf_layout),
+               "moe_finalize_rmsnorm_nvfp4_plan_ex")
+        self._h = h
+
+    def sf_bytes(self) -> int:
+        """Bytes of out_sf in this plan's layout."""
+        return int(self._lib.moe_finalize_rmsnorm_nvfp4_sf_bytes(self._h))
 
     def run(self, expert_out, permuted_row_of, topk_weights, residual_in, residual_out, gamma, eps: float,
             s_enc: float, out_q, out_sf, stream=None, *, validate: bool = True):
@@ -313,10 +339,14 @@ class Nvfp4Plan(Plan):
                                        ("residual_in", residual_in, torch.float32, (T, H)),
                                        ("residual_out", residual_out, torch.float32, (T, H)),
                                        ("gamma", gamma, torch.bfloat16, (H,)),
-                                       ("out_q", out_q, torch.uint8, (T, H // 2)),
-                                       ("out_sf", out_sf, torch.uint8, (T, H // 16))]:
+                                       ("out_q", out_q, torch.uint8, (T, H // 2))] + \
+                    ([("out_sf", out_sf, torch.uint8, (T, H // 16))] if self.sf_layout == SF_ROW_MAJOR else []):
                 if t.dtype != dt or tuple(t.shape) != shape or not t.is_cuda or not t.is_contiguous():
                     raise ValueError(f"{name}: expected contiguous CUDA {dt} {shape}")
+            if self.sf_layout != SF_ROW_MAJOR and (out_sf.dtype != torch.uint8 or out_sf.numel() != self.sf_bytes()
+                                                   or not out_sf.is_cuda or not out_sf.is_contiguous()):
+                raise ValueError(f"out_sf: expected a contiguous CUDA uint8 tensor of {self.sf_bytes()} bytes "
+                                 "(the tiled block-scale layout)")
         code = self._lib.moe_finalize_rmsnorm_nvfp4_run(
             self._h, _ptr(expert_out), _ptr(permuted_row_of), _ptr(topk_weights), _ptr(residual_in),
             _ptr(residual_out), _ptr(gamma), ctypes.c_float(eps), ctypes.c_float(s_enc), _ptr(out_q),

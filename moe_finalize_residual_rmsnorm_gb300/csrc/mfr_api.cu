@@ -24,6 +24,7 @@ struct mfr_plan_s {
     bool fused;        // residual + RMSNorm (false: moe_finalize_plan's plain finalize)
     bool fp4;          // made by moe_finalize_rmsnorm_nvfp4_plan: NVFP4 output
     bool expert_norm;  // made by moe_finalize_expert_rmsnorm_plan
+    int sf_layout;     // NVFP4 plans: MFR_SF_ROW_MAJOR or MFR_SF_TILED_128x4
 };
 
 namespace {
@@ -85,7 +86,7 @@ namespace {
 
 // Shared by the fused plan (residual + RMSNorm) and the plain-finalize plan.
 int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mfr_options* opt,
-              bool fused, bool fp4, bool expert_norm = false) {
+              bool fused, bool fp4, bool expert_norm = false, int sf_layout = MFR_SF_ROW_MAJOR) {
     g_last_error[0] = '\0';
     if (!plan) return fail(MFR_ERR_INVALID_ARG, "plan must not be NULL");
     *plan = nullptr;
@@ -142,6 +143,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     l.fused = fused ? 1 : 0;
     l.fp4 = fp4 ? 1 : 0;
     l.expert_norm = expert_norm ? 1 : 0;
+    l.sf_tiled = (fp4 && sf_layout == MFR_SF_TILED_128x4) ? 1 : 0;
     l.variant = pol.variant;
     l.early_trigger = pol.early_trigger;
     l.cluster = pol.cluster;
@@ -154,7 +156,8 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         l.smem_bytes = mfr::stream_smem_bytes(k, stages, fused);
         // the attribute is per kernel, shared by every plan: always the device
         // maximum, so a plan with a deeper ring never loses its setting
-        if ((e = mfr::stream_prepare(static_cast<int>(H), fused, fp4, ring_budget, expert_norm)) != cudaSuccess) {
+        if ((e = mfr::stream_prepare(static_cast<int>(H), fused, fp4, ring_budget, expert_norm, l.sf_tiled != 0)) !=
+            cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);
         }
@@ -243,6 +246,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     p->fused = fused;
     p->fp4 = fp4;
     p->expert_norm = expert_norm;
+    p->sf_layout = sf_layout;
     *plan = p;
     return MFR_OK;
 }
@@ -259,6 +263,23 @@ int moe_finalize_rmsnorm_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int
 int moe_finalize_rmsnorm_nvfp4_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
                                     const mfr_options* opt) {
     return make_plan(plan, T, H, k, R, opt, true, true);
+}
+
+int moe_finalize_rmsnorm_nvfp4_plan_ex(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R,
+                                       const mfr_options* opt, int sf_layout) {
+    if (sf_layout != MFR_SF_ROW_MAJOR && sf_layout != MFR_SF_TILED_128x4) {
+        if (plan) *plan = nullptr;
+        return fail(MFR_ERR_INVALID_ARG, "sf_layout %d is not MFR_SF_ROW_MAJOR or MFR_SF_TILED_128x4", sf_layout);
+    }
+    return make_plan(plan, T, H, k, R, opt, true, true, false, sf_layout);
+}
+
+int64_t moe_finalize_rmsnorm_nvfp4_sf_bytes(mfr_plan_t plan) {
+    if (!plan || !plan->fp4) return -1;
+    const int64_t S = plan->H / 16;
+    if (plan->sf_layout == MFR_SF_TILED_128x4)
+        return (plan->T + 127) / 128 * 128 * ((S + 3) / 4 * 4);
+    return plan->T * S;
 }
 
 int moe_finalize_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mfr_options* opt) {
@@ -428,7 +449,8 @@ int fused_run(mfr_plan_t plan, const void* expert_out, const int32_t* permuted_r
         return fail(MFR_ERR_INVALID_ARG, "residual_out overlaps an input");
     // every output region against every other argument
     const void* outs[2] = {fp4 ? out_q : out, fp4 ? out_sf : nullptr};
-    const size_t out_bytes[2] = {fp4 ? n_out / 4 : n_out, fp4 ? static_cast<size_t>(T * H) / 16 : 0};
+    const size_t out_bytes[2] = {fp4 ? n_out / 4 : n_out,
+                                 fp4 ? static_cast<size_t>(moe_finalize_rmsnorm_nvfp4_sf_bytes(plan)) : 0};
     for (int o = 0; o < 2; ++o) {
         if (!outs[o]) continue;
         if (overlaps(outs[o], out_bytes[o], expert_out, n_e) || overlaps(outs[o], out_bytes[o], permuted_row_of, n_tk) ||

@@ -165,6 +165,18 @@ __device__ __forceinline__ uint32_t e2m1x2_rn_sat(float lo, float hi) {
     return q & 0xFFu;
 }
 
+// Byte index of the block scale of row t, block b (S blocks per row) in the
+// NVFP4 output: row-major [T, S], or (tiled) the layout block-scaled FP4
+// GEMMs read: the scale matrix padded to multiples of 128 rows and 4 columns
+// is cut into 128 x 4 tiles of 512 consecutive bytes, tiles in row-major
+// order, and scale (r, c) of a tile sits at byte (r mod 32) * 16 +
+// ((r / 32) mod 4) * 4 + (c mod 4).
+__device__ __forceinline__ int64_t nvfp4_sf_index(int64_t t, int b, int S, int tiled) {
+    if (!tiled) return t * S + b;
+    const int64_t tile = (t >> 7) * ((S + 3) >> 2) + (b >> 2);
+    return tile * 512 + (t & 31) * 16 + ((t >> 5) & 3) * 4 + (b & 3);
+}
+
 // NVFP4 of a 16-element block held by a lane pair (lanes 2m and 2m+1, eight
 // values each, lane 2m holding the first eight).  All 32 lanes must call it.
 //   amax = max |y|;  sf = E4M3((amax / 6) * s_enc);  dec = value(sf) / s_enc;

@@ -19,7 +19,7 @@ struct Params {
     const uint16_t* gamma;          // bf16 bits [H]
     uint16_t* out;                  // bf16 bits [T, H]
     uint8_t* out_q;                 // NVFP4 codes [T, H/2] (NVFP4 plans)
-    uint8_t* out_sf;                // NVFP4 block scales, E4M3 [T, H/16] (NVFP4 plans)
+    uint8_t* out_sf;                // NVFP4 block scales, E4M3: [T, H/16] row-major, or tiled (Launch::sf_tiled)
     float s_enc;                    // NVFP4 tensor scale
     int* status;                    // device status word (MFR_STATUS_* bits)
     int64_t T;
@@ -48,6 +48,7 @@ struct Launch {
     int regslots;     // one-CTA-per-token kernels: slot rows/weights held in registers
     int expert_norm;  // 1: RMSNorm per expert row before the weighted sum (mfr_expert_norm.cu)
     int prefetch_out; // 1: the fused bf16 kernel also prefetches its output lines (smallest calls)
+    int sf_tiled;     // NVFP4: 1 = block scales in the 128 x 4 tiles block-scaled GEMMs read
 };
 
 // Sets the calling thread's moe_finalize_rmsnorm_last_error() text.
@@ -83,7 +84,7 @@ cudaError_t expert_norm_launch(const Params& p, const Launch& l, cudaStream_t s)
 int stream_threads();
 int stream_stage_bytes(int k, bool fused);
 int stream_smem_bytes(int k, int nstages, bool fused);
-cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en = false);
+cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en = false, bool sf_tiled = false);
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s);
 
 }  // namespace mfr

@@ -53,7 +53,7 @@ namespace {
 // PFO: also ask L2 for the output lines before the wait (the smallest fused
 // bf16 calls, see kPrefetchOutMaxElems; a separate instantiation, so larger
 // calls keep the code they were tuned with).
-template <int CPT, int SG, bool FUSED, bool FP4, bool RS, bool PFO = false>
+template <int CPT, int SG, bool FUSED, bool FP4, bool RS, bool PFO = false, bool SFT = false>
 __global__ void __launch_bounds__(kRowsMaxThreads)
 rows_kernel(const Params p, const int csize)
 {
@@ -293,7 +293,8 @@ rows_kernel(const Params p, const int csize)
             if (c < nck) {
                 const int64_t col = col0 + static_cast<int64_t>(c) * 8;
                 *reinterpret_cast<uint32_t*>(p.out_q + t * (p.H / 2) + col / 2) = w;
-                if ((c & 1) == 0) p.out_sf[t * (p.H / 16) + col / 16] = static_cast<uint8_t>(sf);
+                if ((c & 1) == 0)
+                    p.out_sf[nvfp4_sf_index(t, static_cast<int>(col / 16), p.H / 16, SFT)] = static_cast<uint8_t>(sf);
             }
         }
         return;
@@ -318,20 +319,23 @@ rows_kernel(const Params p, const int csize)
 using RowsKernel = void (*)(const Params, const int);
 
 template <int CPT, int SG, bool RS>
-RowsKernel pick_rows(bool fused, bool fp4) {
-    if (fp4) return fused ? rows_kernel<CPT, SG, true, true, RS> : nullptr;
+RowsKernel pick_rows(bool fused, bool fp4, bool sft) {
+    if (fp4) {
+        if (!fused) return nullptr;
+        return sft ? rows_kernel<CPT, SG, true, true, RS, false, true> : rows_kernel<CPT, SG, true, true, RS>;
+    }
     return fused ? rows_kernel<CPT, SG, true, false, RS> : rows_kernel<CPT, SG, false, false, RS>;
 }
 
 // Shared-memory slot reads (RS = false) are instantiated only for one chunk
 // per thread: the only case where the registers cost residency (512-thread
 // CTAs at 64 vs 112 registers per thread).
-RowsKernel rows_kernel_for(int cpt, bool fused, bool fp4, bool regslots, bool pfo = false) {
+RowsKernel rows_kernel_for(int cpt, bool fused, bool fp4, bool regslots, bool pfo = false, bool sft = false) {
     if (pfo) return (cpt == 1 && fused && !fp4 && regslots) ? rows_kernel<1, 8, true, false, true, true> : nullptr;
     switch (cpt) {
-        case 1: return regslots ? pick_rows<1, 8, true>(fused, fp4) : pick_rows<1, 8, false>(fused, fp4);
-        case 2: return regslots ? pick_rows<2, 8, true>(fused, fp4) : nullptr;
-        case 4: return regslots ? pick_rows<4, 2, true>(fused, fp4) : nullptr;
+        case 1: return regslots ? pick_rows<1, 8, true>(fused, fp4, sft) : pick_rows<1, 8, false>(fused, fp4, sft);
+        case 2: return regslots ? pick_rows<2, 8, true>(fused, fp4, sft) : nullptr;
+        case 4: return regslots ? pick_rows<4, 2, true>(fused, fp4, sft) : nullptr;
         default: return nullptr;
     }
 }
@@ -530,13 +534,14 @@ cudaError_t floor_work_launch(const Params& p, const Launch& l, int work, cudaSt
 bool rows_supported_cpt(int cpt) { return rows_kernel_for(cpt, true, false, true) != nullptr; }
 
 cudaError_t rows_blocks_per_sm(const Launch& l, bool regslots, int* n) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, regslots);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, regslots, false, l.sf_tiled != 0);
     if (!k) { *n = 0; return cudaSuccess; }
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k, l.block, static_cast<size_t>(l.smem_bytes));
 }
 
 cudaError_t rows_prepare(const Launch& l) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0, l.prefetch_out != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0, l.prefetch_out != 0,
+                                   l.sf_tiled != 0);
     if (!k) return cudaErrorInvalidValue;
     if (l.cluster > 8 && l.fused)
         return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -544,7 +549,8 @@ cudaError_t rows_prepare(const Launch& l) {
 }
 
 cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0, l.prefetch_out != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0, l.prefetch_out != 0,
+                                   l.sf_tiled != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];
@@ -553,7 +559,8 @@ cudaError_t rows_max_active_clusters(const Launch& l, int* n) {
 }
 
 cudaError_t rows_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0, l.prefetch_out != 0);
+    RowsKernel k = rows_kernel_for(l.cpt, l.fused != 0, l.fp4 != 0, l.regslots != 0, l.prefetch_out != 0,
+                                   l.sf_tiled != 0);
     if (!k) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];

@@ -67,8 +67,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 // MAXTILES: upper bound on ceil(H / CB) for this instantiation;
 // FUSED: residual + RMSNorm (true) or plain finalize (false); EN: per-expert
-// RMSNorm (with FUSED = false).
-template <int MAXTILES, bool FUSED, bool FP4, bool EN>
+// RMSNorm (with FUSED = false); SFT (with FP4): block scales in the tiled
+// layout of block-scaled GEMMs instead of row-major.
+template <int MAXTILES, bool FUSED, bool FP4, bool EN, bool SFT = false>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 stream_kernel(const Params p, const int nstages, const int stage_bytes)
 {
@@ -489,7 +490,8 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 const uint32_t w = nvfp4_block4(y, p.s_enc, s_enc_tab, &sf);
                 if (col < H) {
                     *reinterpret_cast<uint16_t*>(p.out_q + t * (H / 2) + col / 2) = static_cast<uint16_t>(w);
-                    if ((tid & 3) == 0) p.out_sf[t * (H / 16) + col / 16] = static_cast<uint8_t>(sf);
+                    if ((tid & 3) == 0)
+                        p.out_sf[nvfp4_sf_index(t, col / 16, H / 16, SFT)] = static_cast<uint8_t>(sf);
                 }
             } else if (col < H) {
                 st_u2(p.out + t * H + col, make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3])));
@@ -502,12 +504,15 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
 using StreamKernel = void (*)(const Params, const int, const int);
 
 template <int MAXTILES>
-StreamKernel pick(bool fused, bool fp4) {
-    if (fp4) return fused ? stream_kernel<MAXTILES, true, true, false> : nullptr;
+StreamKernel pick(bool fused, bool fp4, bool sft) {
+    if (fp4) {
+        if (!fused) return nullptr;
+        return sft ? stream_kernel<MAXTILES, true, true, false, true> : stream_kernel<MAXTILES, true, true, false>;
+    }
     return fused ? stream_kernel<MAXTILES, true, false, false> : stream_kernel<MAXTILES, false, false, false>;
 }
 
-StreamKernel stream_kernel_for(int H, bool fused, bool fp4, bool en) {
+StreamKernel stream_kernel_for(int H, bool fused, bool fp4, bool en, bool sft = false) {
     const int tiles = (H + kStreamCB - 1) / kStreamCB;
     if (en) {
         if (fused || fp4) return nullptr;
@@ -515,9 +520,9 @@ StreamKernel stream_kernel_for(int H, bool fused, bool fp4, bool en) {
         if (tiles <= 4) return stream_kernel<4, false, false, true>;
         return nullptr;
     }
-    if (tiles <= 2) return pick<2>(fused, fp4);
-    if (tiles <= 4) return pick<4>(fused, fp4);
-    if (tiles <= 8) return pick<8>(fused, fp4);
+    if (tiles <= 2) return pick<2>(fused, fp4, sft);
+    if (tiles <= 4) return pick<4>(fused, fp4, sft);
+    if (tiles <= 8) return pick<8>(fused, fp4, sft);
     return nullptr;
 }
 
@@ -533,14 +538,14 @@ int stream_smem_bytes(int k, int nstages, bool fused) {
     return ((2 * nstages * 8 + 127) / 128) * 128 + nstages * stream_stage_bytes(k, fused);
 }
 
-cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en) {
-    StreamKernel kf = stream_kernel_for(H, fused, fp4, en);
+cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en, bool sf_tiled) {
+    StreamKernel kf = stream_kernel_for(H, fused, fp4, en, sf_tiled);
     if (!kf) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    StreamKernel kf = stream_kernel_for(p.H, l.fused != 0, l.fp4 != 0, l.expert_norm != 0);
+    StreamKernel kf = stream_kernel_for(p.H, l.fused != 0, l.fp4 != 0, l.expert_norm != 0, l.sf_tiled != 0);
     if (!kf) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid_x), 1, 1);

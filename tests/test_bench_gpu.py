@@ -44,7 +44,9 @@ def test_gpu_arm_prints_the_contract_line():
     assert [r["T"] for r in sw["decode"]] == [1, 2, 4, 8]
     for r in sw["decode"]:
         assert r["H"] == 4096 and r["replays"] >= 21 and r["floor_us"] > 0 and r["us_per_call"] > r["floor_us"]
-        assert abs(r["vs_2x_floor"] - r["us_per_call"] / (2 * (r["floor_us"] + r["T"] * 106560 / 8e12 * 1e6))) < 2e-3
+        # the line rounds each figure to 3 decimals: recomputed from them, within 0.5 %
+        want = r["us_per_call"] / (2 * (r["floor_us"] + r["T"] * 106560 / 8e12 * 1e6))
+        assert abs(r["vs_2x_floor"] - want) <= 5e-3 * want
     assert [(r["T"], r["H"]) for r in sw["bandwidth"]] == [(512, 8192), (4096, 8192), (8192, 8192), (32768, 8192)]
     assert all(0 < r["frac"] < 1.5 for r in sw["bandwidth"])
     assert sw["bandwidth"][-1]["bitwise_repeat"] is True

@@ -143,3 +143,110 @@ def test_nvfp4_argument_checks():
         mfr.Plan.run(plan, inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], inp["residual"],
                      rout, inp["gamma"], 1e-6, torch.empty((4, 4096), dtype=torch.bfloat16, device="cuda"))
     torch.cuda.synchronize()
+
+
+# ---- block scales in the tiled layout of block-scaled FP4 GEMMs ----------------------
+
+PAD = 0xEE
+
+
+def _tile_offsets(T, S):
+    """offsets[r, c]: the byte of scale (r, c) in the tiled layout, from the
+    oracle's layout map applied to the scales' own indices."""
+    idx = np.arange(T * S, dtype=np.int64).reshape(T, S)
+    lo = oracle.nvfp4_swizzle_scales((idx & 0xFF).astype(np.uint8))
+    mid = oracle.nvfp4_swizzle_scales(((idx >> 8) & 0xFF).astype(np.uint8))
+    hi = oracle.nvfp4_swizzle_scales(((idx >> 16) & 0xFF).astype(np.uint8))
+    flat = lo.astype(np.int64) | (mid.astype(np.int64) << 8) | (hi.astype(np.int64) << 16)
+    written = np.zeros(flat.size, dtype=bool)
+    written[oracle.nvfp4_swizzle_scales(np.ones((T, S), dtype=np.uint8), fill=0) == 1] = True
+    offsets = np.empty(T * S, dtype=np.int64)
+    offsets[flat[written]] = np.flatnonzero(written)
+    return offsets.reshape(T, S), written
+
+
+def run_nvfp4_tiled(inp, s_enc, **kw):
+    e = inp["expert_out"]
+    T, k = inp["permuted_row_of"].shape
+    R, H = e.shape
+    plan = mfr.Nvfp4Plan(T, H, k, R, sf_layout=mfr.SF_TILED_128x4, **kw)
+    n = plan.sf_bytes()
+    assert n == -(-T // 128) * 128 * (-(-(H // 16) // 4) * 4)
+    G = 64
+    qb = torch.full((T * H // 2 + 2 * G,), 0xA5, dtype=torch.uint8, device="cuda")
+    sb = torch.full((n + 2 * G,), PAD, dtype=torch.uint8, device="cuda")
+    out_q, out_sf = qb[G:G + T * H // 2].view(T, H // 2), sb[G:G + n]
+    rout = torch.empty_like(inp["residual"])
+    plan.run(e, inp["permuted_row_of"], inp["topk_weights"], inp["residual"], rout, inp["gamma"], inp["eps"],
+             s_enc, out_q, out_sf)
+    torch.cuda.synchronize()
+    assert torch.all(qb[:G] == 0xA5) and torch.all(qb[-G:] == 0xA5), "write outside out_q"
+    assert torch.all(sb[:G] == PAD) and torch.all(sb[-G:] == PAD), "write outside out_sf"
+    return f32(rout), out_q.cpu().numpy(), out_sf.cpu().numpy(), plan
+
+
+TILED_CASES = [
+    ("decode_T1_cluster", W.decode(1), {}),
+    ("decode_T8_cluster", W.decode(8), {}),
+    ("prefill_T300_rows", W.PREFILL.with_(T=300), {}),
+    ("prefill_T2000_stream", W.PREFILL.with_(T=2000), {}),
+    ("wide_T129_stream", W.wide(129), dict(variant=mfr.VARIANT_STREAM)),
+    ("H1040_T7_cluster", W.Workload("h1040", T=7, H=1040, k=5, E=16), dict(variant=mfr.VARIANT_CLUSTER)),
+    ("H16384_T5", W.Workload("h16k", T=5, H=16384, k=8, E=32), {}),
+]
+
+
+@pytest.mark.parametrize("name,wl,kw", TILED_CASES, ids=[c[0] for c in TILED_CASES])
+def test_nvfp4_tiled_scales(name, wl, kw):
+    """The tiled plan writes every scale where the oracle's layout map puts
+    it, leaves the padding alone, and its codes and scales are the row-major
+    plan's, byte for byte (and pass the oracle check)."""
+    inp = W.make_inputs(wl, "cuda")
+    x_o, y32 = _oracle_y32(inp)
+    s_enc = _s_enc(y32)
+    res, q, sf_tiled, plan = run_nvfp4_tiled(inp, s_enc, **kw)
+    offsets, written = _tile_offsets(wl.T, wl.H // 16)
+    assert np.all(sf_tiled[~written] == PAD), "a padding byte of the scale tiles was written"
+    sf = sf_tiled[offsets]
+    assert_residual_close(res, x_o)
+    check_nvfp4(y32, s_enc, q, sf)
+    _, q_rm, sf_rm, _ = run_nvfp4(inp, s_enc, **kw)
+    assert np.array_equal(q, q_rm) and np.array_equal(sf, sf_rm)
+    assert plan.get_status() == 0
+
+
+def test_nvfp4_tiled_output_feeds_a_block_scaled_gemm():
+    """out_q with its tiled scales, handed to a block-scaled FP4 GEMM
+    (torch._scaled_mm through cuBLASLt) as the A operand, gives the product
+    of the dequantised values: the layout is the one such GEMMs read."""
+    if not hasattr(torch, "float4_e2m1fn_x2"):
+        pytest.skip("this torch has no FP4 dtype")
+    wl = W.PREFILL.with_(T=256)
+    inp = W.make_inputs(wl, "cuda")
+    _, y32 = _oracle_y32(inp)
+    s_enc = _s_enc(y32)
+    _, q, sf_tiled, _ = run_nvfp4_tiled(inp, s_enc)
+    T, H, N = wl.T, wl.H, 128
+    rng = np.random.default_rng(3)
+    b_codes = rng.integers(0, 16, (N, H)).astype(np.uint8)
+    b_sf = rng.integers(0x30, 0x40, (N, H // 16)).astype(np.uint8)
+    b_packed = (b_codes[:, 0::2] | (b_codes[:, 1::2] << 4)).astype(np.uint8)
+    e2m1 = oracle.default().e2m1_to_f64(np.arange(16, dtype=np.uint8))
+    e4m3 = oracle.default().e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    offsets, _ = _tile_offsets(T, H // 16)
+    a = e2m1[oracle.unpack_e2m1(q)] * np.repeat(e4m3[sf_tiled[offsets]], 16, axis=1)
+    b = e2m1[b_codes] * np.repeat(e4m3[b_sf], 16, axis=1)
+    want = a @ b.T
+    ta = torch.from_numpy(q).cuda().view(torch.float4_e2m1fn_x2)
+    tb = torch.from_numpy(b_packed).cuda().view(torch.float4_e2m1fn_x2)
+    sa = torch.from_numpy(sf_tiled).cuda().view(torch.float8_e4m3fn)
+    sb = torch.from_numpy(oracle.nvfp4_swizzle_scales(b_sf)).cuda().view(torch.float8_e4m3fn)
+    try:
+        got = torch._scaled_mm(ta, tb.t(), sa, sb, out_dtype=torch.float32)
+    except (RuntimeError, NotImplementedError, TypeError) as e:
+        pytest.skip(f"no block-scaled FP4 GEMM in this torch build: {e}")
+    got = got.cpu().double().numpy()
+    # FP32 accumulation of H products in any order: within H * 2^-24 of the
+    # sum of their magnitudes (a wrong scale layout misses by O(1))
+    bound = H * 2.0 ** -24 * (np.abs(a) @ np.abs(b).T)
+    assert np.all(np.abs(got - want) <= bound + 1e-30)
