@@ -193,6 +193,8 @@ TILED_CASES = [
     ("wide_T129_stream", W.wide(129), dict(variant=mfr.VARIANT_STREAM)),
     ("H1040_T7_cluster", W.Workload("h1040", T=7, H=1040, k=5, E=16), dict(variant=mfr.VARIANT_CLUSTER)),
     ("H16384_T5", W.Workload("h16k", T=5, H=16384, k=8, E=32), {}),
+    ("H4112_T700_stream", W.Workload("h4112", T=700, H=4112, k=8, E=64), dict(variant=mfr.VARIANT_STREAM)),
+    ("H4144_T300_stream", W.Workload("h4144", T=300, H=4144, k=6, E=48), dict(variant=mfr.VARIANT_STREAM)),
 ]
 
 
