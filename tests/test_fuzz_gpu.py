@@ -1,6 +1,6 @@
 """Random shapes and options against the oracle: every output kind (fused,
-plain finalize, NVFP4, per-expert RMSNorm) under every variant that takes the
-shape, with seeded draws of T, H, k, the variant and the cluster size.  The
+plain finalize, NVFP4 with row-major or tiled block scales, per-expert
+RMSNorm) under every variant that takes the shape, with seeded draws of T, H, k, the variant and the cluster size.  The
 bars are the ones of the per-kind parity tests; the point here is breadth of
 shapes (ragged H, any k from 1 to 16, token counts around the thresholds)."""
 import numpy as np
@@ -12,7 +12,7 @@ import workloads as W
 from helpers import assert_out_close, assert_residual_close, oracle_finalize_only, oracle_expert_norm
 from test_expert_norm_gpu import assert_expert_norm_close, run_expert_norm
 from test_finalize_only_gpu import run_finalize
-from test_nvfp4_gpu import _oracle_y32, _s_enc, check_nvfp4, run_nvfp4
+from test_nvfp4_gpu import PAD, _oracle_y32, _s_enc, _tile_offsets, check_nvfp4, run_nvfp4, run_nvfp4_tiled
 from test_parity_gpu import compare_full
 
 pytestmark = pytest.mark.gpu
@@ -65,7 +65,13 @@ def test_random_shape_matches_oracle(kind, T, H, k, variant, cluster, seed):
         elif kind == "nvfp4":
             x_o, y32 = _oracle_y32(inp)
             s_enc = _s_enc(y32)
-            res, q, sf, plan = run_nvfp4(inp, s_enc, **kw)
+            if seed % 2:             # half of the NVFP4 cases write their scales in the tiled layout
+                res, q, sf_tiled, plan = run_nvfp4_tiled(inp, s_enc, **kw)
+                offsets, written = _tile_offsets(T, H // 16)
+                assert np.all(sf_tiled[~written] == PAD)
+                sf = sf_tiled[offsets]
+            else:
+                res, q, sf, plan = run_nvfp4(inp, s_enc, **kw)
             assert_residual_close(res, x_o)
             check_nvfp4(y32, s_enc, q, sf, max_ambiguous=0.05)
             assert plan.get_status() == 0
