@@ -65,11 +65,11 @@ def parse_args(argv=None):
                     help="also time the full decode and wide sweeps (graph, stream loop, warm L2, other outputs)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the compact sweep of the metric (decode T<=8 against its floor, wide H=8192, "
-                         "stress) that the JSON line carries by default")
+                         "stress), the other outputs and the producer pairs that the line carries by default")
     ap.add_argument("--variants", action="store_true",
-                    help="also time the plain finalize and the NVFP4 epilogue on the headline workload")
+                    help="time the other outputs on the headline workload even with --no-sweep")
     ap.add_argument("--pdl-pairs", action="store_true",
-                    help="also time producer -> finalize pairs with and without dependent launch")
+                    help="time producer -> finalize pairs even with --no-sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -407,9 +407,12 @@ def run_ours(args):
         result["sweep"] = run_compact_sweep(mfr, device, args)
     if args.sweep:
         result["sweep_full"] = run_sweep(mfr, device, args)
-    if args.pdl_pairs:
+    # the other outputs on the headline workload and the producer -> finalize
+    # pairs ride on the default line too (rank 0), unless --no-sweep
+    default_extras = rank == 0 and not args.no_sweep and not args.tokens
+    if args.pdl_pairs or default_extras:
         result["pdl_pairs"] = run_pdl_pairs(mfr, device)
-    if args.variants:
+    if args.variants or default_extras:
         result["variants"] = run_variants(mfr, device, wl, sets, args)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(host_copy(sets[0]), wl, args.cpu_seconds)
@@ -960,7 +963,9 @@ def run_pdl_pairs(mfr, device):
     and without programmatic dependent launch.  The stand-in producer waits,
     signals its dependents, stays busy for `busy` cycles (a GEMM's main loop),
     then writes expert_out; with PDL the finalize's launch and prologue hide
-    behind it.  Input sets rotate so the finalize reads cold residual data."""
+    behind it.  Every pair uses the same buffers: the producer rewrites
+    expert_out before each finalize, and the residual is the same tensor in
+    every pair (for small T it stays in L2)."""
     rows = []
     for wl in (W.decode(1), W.decode(8), W.decode(128), W.PREFILL):
         base = W.make_inputs(wl, device)

@@ -50,6 +50,10 @@ def test_gpu_arm_prints_the_contract_line():
     assert [(r["T"], r["H"]) for r in sw["bandwidth"]] == [(512, 8192), (4096, 8192), (8192, 8192), (32768, 8192)]
     assert all(0 < r["frac"] < 1.5 for r in sw["bandwidth"])
     assert sw["bandwidth"][-1]["bitwise_repeat"] is True
+    # so do the other outputs and the producer -> finalize pairs
+    assert set(d["variants"]) == {"finalize_only", "nvfp4_epilogue", "nvfp4_epilogue_tiled_scales", "expert_rmsnorm"}
+    assert all(v["us_per_call"] > 0 for v in d["variants"].values())
+    assert {(r["T"], r["busy_cycles"]) for r in d["pdl_pairs"]} >= {(1, 0), (8, 0)}
     ref = run_bench("--impl", "reference", "--workload", "decode_T8", "--steps", "3", "--warmup", "3",
                     "--cpu-seconds", "0.05")
     shared = {k: v for k, v in ref["config"].items() if k != "bytes_per_call"}
