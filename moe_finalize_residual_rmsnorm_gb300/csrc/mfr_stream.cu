@@ -119,8 +119,12 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
         // copy, which caps the plain finalize at 4.8 TB/s (224 us) and parallel
         // issue lifts it to 174 us; the residual + bf16-out form instead runs
         // 6 % faster from one lane (246 vs 263 us, its writes compete with a
-        // faster read stream), and the NVFP4 form 1.4 % faster in parallel.
-        constexpr bool kParallelIssue = !FUSED || FP4;
+        // faster read stream).  The NVFP4 form is 1.4 % faster in parallel at
+        // H = 4096 (two tiles per token), but from one lane with four or more
+        // tiles (measured: H = 8192 at T = 4096 / 8192 2.8 / 3.5 % faster,
+        // T = 16384 with the stress routing 4.3 %, H = 16384 at T = 2048
+        // 3.8 %).
+        constexpr bool kParallelIssue = !FUSED || (FP4 && MAXTILES <= 2);
         // The residual + bf16 form with four or more tiles per token (H > 4096)
         // issues the first two fills of its ring from the slots' own lanes and
         // the rest from one lane.  Measured on two GB300s against one-lane
