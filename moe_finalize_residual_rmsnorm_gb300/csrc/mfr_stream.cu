@@ -198,14 +198,15 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
 #pragma unroll
                     for (int j = 0; j < kMaxK; ++j) rl[j] = __shfl_sync(0xFFFFFFFFu, row, j);
                     if (lane == 0) {
+                        // the residual segment first (measured: prefill 246.1 -> 245.3 us)
+                        if (FUSED)   // only fused stages carry a residual segment (and count its bytes)
+                            bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
 #pragma unroll
                         for (int j = 0; j < kMaxK; ++j)
                             if (mask & (1u << j))
                                 bulk_g2s(smem_u32(st + kHeaderBytes + j * row_bytes),
                                          p.expert_out + static_cast<int64_t>(rl[j]) * H + c0,
                                          static_cast<uint32_t>(cb * 2), bar);
-                        if (FUSED)   // only fused stages carry a residual segment (and count its bytes)
-                            bulk_g2s(smem_u32(st + res_off), p.residual_in + t * H + c0, static_cast<uint32_t>(cb * 4), bar);
                     }
                 }
                 ++fill;
