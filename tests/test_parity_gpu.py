@@ -435,3 +435,29 @@ def test_every_slot_non_local(kw):
         torch.cuda.synchronize()
         assert torch.all(out.float() == 0)
         assert p.get_status() == 0
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(variant=mfr.VARIANT_ROWS), dict(variant=mfr.VARIANT_STREAM)],
+                         ids=["auto_cluster", "rows", "stream"])
+def test_one_plan_on_four_streams_at_once(kw):
+    """A plan is immutable: one plan runs on four streams at the same time,
+    each call on its own inputs, and every call matches the oracle."""
+    T = 64 if not kw else 300
+    calls = [W.make_inputs(W.PREFILL.with_(T=T, seed=40 + i), "cuda") for i in range(4)]
+    plan = mfr.Plan(T, 4096, 8, T * 8, **kw)
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    outs = []
+    torch.cuda.synchronize()
+    for inp, s in zip(calls, streams):
+        rout = torch.empty_like(inp["residual"])
+        out = torch.empty((T, 4096), dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):        # a few calls per stream, all in flight together
+            plan.run(inp["expert_out"], inp["permuted_row_of"], inp["topk_weights"], inp["residual"], rout,
+                     inp["gamma"], inp["eps"], out, s)
+        outs.append((rout, out))
+    torch.cuda.synchronize()
+    for inp, (rout, out) in zip(calls, outs):
+        want_res, want_out, _ = oracle_on(inp)
+        assert_residual_close(f32(rout), want_res)
+        assert_out_close(bf16_bits(out), want_out)
+    assert plan.get_status() == 0
