@@ -157,22 +157,31 @@ rows_kernel(const Params p, const int csize)
     pdl_wait();
 
     // ---- residual row and the k expert rows ---------------------------------
+    // The smallest calls (PFO) issue the residual loads after the first slot
+    // group's row loads, so the rows that the first FMAs need come back first
+    // (measured: T = 1 / 2 / 4 at H = 4096 3.3 / 3.9 / 3.1 % faster); the same
+    // order made the other instantiations 11-24 % slower (T = 8 ... 128), so
+    // they load the residual first.
+    constexpr bool kResidualAfterRows = PFO;
     float res[CPT][8];
+    auto load_residual = [&]() {
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-        const int c = tid + i * nthreads;
-        const int cc = c < nck ? c : 0;
-        if (FUSED) {
-            const float* res_in = p.residual_in + t * p.H + col0;
-            const float4 a = ld_once_f4(res_in + cc * 8);
-            const float4 b = ld_once_f4(res_in + cc * 8 + 4);
-            res[i][0] = a.x; res[i][1] = a.y; res[i][2] = a.z; res[i][3] = a.w;
-            res[i][4] = b.x; res[i][5] = b.y; res[i][6] = b.z; res[i][7] = b.w;
-        } else {
+        for (int i = 0; i < CPT; ++i) {
+            const int c = tid + i * nthreads;
+            const int cc = c < nck ? c : 0;
+            if (FUSED) {
+                const float* res_in = p.residual_in + t * p.H + col0;
+                const float4 a = ld_once_f4(res_in + cc * 8);
+                const float4 b = ld_once_f4(res_in + cc * 8 + 4);
+                res[i][0] = a.x; res[i][1] = a.y; res[i][2] = a.z; res[i][3] = a.w;
+                res[i][4] = b.x; res[i][5] = b.y; res[i][6] = b.z; res[i][7] = b.w;
+            } else {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) res[i][q] = 0.f;
+                for (int q = 0; q < 8; ++q) res[i][q] = 0.f;
+            }
         }
-    }
+    };
+    if constexpr (!kResidualAfterRows) load_residual();
 
     float acc[CPT][8];
 #pragma unroll
@@ -196,6 +205,9 @@ rows_kernel(const Params p, const int csize)
                 v[s][i] = make_uint4(0, 0, 0, 0);
                 if (r >= 0) v[s][i] = ld_stream_u4(row + (c < nck ? c : 0) * 8);
             }
+        }
+        if constexpr (kResidualAfterRows) {
+            if (j0 == 0) load_residual();   // after the first group's row loads, before any FMA
         }
 #pragma unroll
         for (int s = 0; s < SG; ++s) {
