@@ -30,14 +30,18 @@ constexpr int64_t kClusterMaxElems = int64_t(1) << 19;
 constexpr int64_t kRowsMaxElems = int64_t(3) << 19;
 constexpr int64_t kEarlyTriggerMaxElems = int64_t(1) << 19;
 // Calls this small leave HBM idle, so the fused bf16 kernel also asks L2 for
-// its output lines before the dependency wait and the stores at the end hit
-// (measured: 3-4 % faster at T <= 4, H = 4096 and T <= 2, H = 8192; 1-4 %
-// slower from 2^15 elements on, where the extra reads compete).  The plain
-// finalize, NVFP4 and per-expert RMSNorm kernels do not: with it they ran
-// 0-8 % slower at the same sizes.  It is a separate instantiation, because
-// merely adding the branch changed the other instantiations' code (T = 8,
-// H = 4096: 1.81 -> 1.84 us without the prefetch taken).
-constexpr int64_t kPrefetchOutMaxElems = int64_t(1) << 14;
+// its output lines before the dependency wait, so the stores at the end hit,
+// and issues its residual loads after its row loads (the rows the first FMAs
+// need come back first).  Measured on GB300: T = 1 / 2 / 4 at H = 4096
+// 3.3-3.9 % faster with the load order, and with the limit at 2^15 rather
+// than 2^14 T = 8 at H = 4096 1.1 % and T = 4 at H = 8192 2.1 % faster,
+// 2^16 no different at T = 16.  The output prefetch alone had been 1-4 %
+// slower from 2^15 elements on.  The plain finalize, NVFP4 and per-expert
+// RMSNorm kernels do not take it: with the output prefetch they ran 0-8 %
+// slower at the same sizes.  It is a separate instantiation, because merely
+// adding the branch changed the other instantiations' code (T = 8, H = 4096:
+// 1.81 -> 1.84 us without the prefetch taken).
+constexpr int64_t kPrefetchOutMaxElems = int64_t(1) << 15;
 
 inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
 

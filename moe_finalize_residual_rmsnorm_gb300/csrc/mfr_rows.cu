@@ -160,8 +160,9 @@ rows_kernel(const Params p, const int csize)
     // The smallest calls (PFO) issue the residual loads after the first slot
     // group's row loads, so the rows that the first FMAs need come back first
     // (measured: T = 1 / 2 / 4 at H = 4096 3.3 / 3.9 / 3.1 % faster); the same
-    // order made the other instantiations 11-24 % slower (T = 8 ... 128), so
-    // they load the residual first.
+    // order in the other instantiations made them 11-24 % slower (T = 8 ...
+    // 128 at H = 4096 before T = 8 moved to this instantiation), so they load
+    // the residual first.
     constexpr bool kResidualAfterRows = PFO;
     float res[CPT][8];
     auto load_residual = [&]() {
