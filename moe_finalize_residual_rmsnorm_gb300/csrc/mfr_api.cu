@@ -202,7 +202,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
             }
             if (without > 0 && waves(without) < waves(with_regs)) l.regslots = 0;
         }
-        l.prefetch_out = (fused && !fp4 && l.cpt == 1 && l.regslots && T * H <= mfr::kPrefetchOutMaxElems) ? 1 : 0;
+        l.prefetch_out = (fused && l.cpt == 1 && l.regslots && T * H <= mfr::kPrefetchOutMaxElems) ? 1 : 0;
         if (!expert_norm && (e = mfr::rows_prepare(l)) != cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);

@@ -47,7 +47,7 @@ struct Launch {
     int early_trigger;  // 1: signal dependents at kernel entry (small grids only)
     int regslots;     // one-CTA-per-token kernels: slot rows/weights held in registers
     int expert_norm;  // 1: RMSNorm per expert row before the weighted sum (mfr_expert_norm.cu)
-    int prefetch_out; // 1: the fused bf16 kernel also prefetches its output lines (smallest calls)
+    int prefetch_out; // 1: the small-call instantiation (residual loads after the rows; bf16 also prefetches its output lines)
     int sf_tiled;     // NVFP4: 1 = block scales in the 128 x 4 tiles block-scaled GEMMs read
 };
 

@@ -50,9 +50,10 @@ namespace {
 // thread holds the slot rows and weights in registers from before the
 // dependency wait (true), or reads them from shared memory as it loads (false:
 // 32 fewer registers, for CTAs whose residency the registers would halve);
-// PFO: also ask L2 for the output lines before the wait (the smallest fused
-// bf16 calls, see kPrefetchOutMaxElems; a separate instantiation, so larger
-// calls keep the code they were tuned with).
+// PFO: the smallest fused calls (see kPrefetchOutMaxElems; a separate
+// instantiation, so larger calls keep the code they were tuned with): the
+// residual loads follow the row loads, and the bf16 form also asks L2 for its
+// output lines before the wait.
 template <int CPT, int SG, bool FUSED, bool FP4, bool RS, bool PFO = false, bool SFT = false>
 __global__ void __launch_bounds__(kRowsMaxThreads)
 rows_kernel(const Params p, const int csize)
@@ -344,7 +345,11 @@ RowsKernel pick_rows(bool fused, bool fp4, bool sft) {
 // per thread: the only case where the registers cost residency (512-thread
 // CTAs at 64 vs 112 registers per thread).
 RowsKernel rows_kernel_for(int cpt, bool fused, bool fp4, bool regslots, bool pfo = false, bool sft = false) {
-    if (pfo) return (cpt == 1 && fused && !fp4 && regslots) ? rows_kernel<1, 8, true, false, true, true> : nullptr;
+    if (pfo) {
+        if (cpt != 1 || !fused || !regslots) return nullptr;
+        if (fp4) return sft ? rows_kernel<1, 8, true, true, true, true, true> : rows_kernel<1, 8, true, true, true, true>;
+        return rows_kernel<1, 8, true, false, true, true>;
+    }
     switch (cpt) {
         case 1: return regslots ? pick_rows<1, 8, true>(fused, fp4, sft) : pick_rows<1, 8, false>(fused, fp4, sft);
         case 2: return regslots ? pick_rows<2, 8, true>(fused, fp4, sft) : nullptr;
