@@ -36,9 +36,11 @@ constexpr int64_t kEarlyTriggerMaxElems = int64_t(1) << 19;
 // 3.3-3.9 % faster with the load order, and with the limit at 2^15 rather
 // than 2^14 T = 8 at H = 4096 1.1 % and T = 4 at H = 8192 2.1 % faster,
 // 2^16 no different at T = 16.  The output prefetch alone had been 1-4 %
-// slower from 2^15 elements on.  The plain finalize, NVFP4 and per-expert
-// RMSNorm kernels do not take it: with the output prefetch they ran 0-8 %
-// slower at the same sizes.  It is a separate instantiation, because merely
+// slower from 2^15 elements on.  The NVFP4 kernel takes the load order but
+// not the output prefetch (T = 1 / 2 / 4 / 8 at H = 4096 1.4 / 1.7 / 1.1 /
+// 0.7 % faster); the plain finalize and per-expert RMSNorm kernels take
+// neither: with the output prefetch they ran 0-8 % slower at the same
+// sizes.  It is a separate instantiation, because merely
 // adding the branch changed the other instantiations' code (T = 8, H = 4096:
 // 1.81 -> 1.84 us without the prefetch taken).
 constexpr int64_t kPrefetchOutMaxElems = int64_t(1) << 15;
