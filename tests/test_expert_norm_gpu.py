@@ -87,6 +87,24 @@ def test_expert_norm_matches_oracle(T, H, k, variant, pdl):
     assert np.array_equal(got, again)
 
 
+@pytest.mark.parametrize("T,H,k", [(2000, 4096, 2), (1200, 8192, 4), (1500, 4096, 7)])
+def test_expert_norm_ring_wraps(T, H, k):
+    """The ring form with fewer than 8 slots (deeper rings) and many tokens
+    per CTA, so the ring wraps many times; at H = 8192 two of a token's four
+    stages are held for the second pass.  Every token against the oracle;
+    a repeated run is bitwise equal."""
+    wl = W.Workload(f"en_ring_T{T}_H{H}_k{k}", T=T, H=H, k=k, E=16, seed=T + H + k, extra_rows=3)
+    inp = W.make_inputs(wl, "cuda")
+    want, y, s, bad = oracle_expert_norm(inp)
+    got, plan = run_expert_norm(inp, variant=mfr.VARIANT_STREAM)
+    assert bad == 0
+    assert_expert_norm_close(got, want, y, s)
+    assert plan.get_status() == 0
+    assert plan.info()["variant"] == mfr.VARIANT_STREAM
+    again, _ = run_expert_norm(inp, plan=plan)
+    assert np.array_equal(got, again)
+
+
 @pytest.mark.parametrize("T,H", [(1, 4096), (3, 8192), (16, 4096), (64, 8192)])
 @pytest.mark.parametrize("cluster", [2, 4, 8, 16])
 def test_expert_norm_every_cluster_size(T, H, cluster):

@@ -55,6 +55,20 @@ def test_finalize_only_matches_oracle(kw, T, H, k):
     assert plan.get_status() == 0
 
 
+@pytest.mark.parametrize("T,H,k", [(2000, 4096, 2), (1500, 8192, 4), (1800, 4096, 16)])
+def test_finalize_only_ring_wraps(T, H, k):
+    """The ring form with ring depths from 3 stages (k = 16) to 8 (k = 2) and
+    many tokens per CTA: every token bitwise equal to the oracle."""
+    wl = W.Workload(f"fin_ring_T{T}_H{H}_k{k}", T=T, H=H, k=k, E=max(16, 2 * k), seed=T + H + k, extra_rows=2)
+    inp = W.make_inputs(wl, "cuda")
+    want, bad = oracle_finalize_only(inp)
+    got, plan = run_finalize(inp, variant=mfr.VARIANT_STREAM)
+    assert bad == 0
+    assert np.array_equal(got, want)
+    assert plan.get_status() == 0
+    assert plan.info()["variant"] == mfr.VARIANT_STREAM
+
+
 @pytest.mark.parametrize("T,H", [(1, 4096), (4, 4096), (2, 8192), (33, 8192)])
 @pytest.mark.parametrize("split", [2, 4, 8, 16])
 def test_finalize_only_every_split(T, H, split):

@@ -73,6 +73,9 @@ CASES = [
     ("decode_T32_cluster8", W.decode(32), {}),                           # 64-thread CTAs at 2^17
     ("decode_T4_cluster16", W.decode(4), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=16)),
     ("wide_T2_cluster16", W.wide(2), dict(variant=mfr.VARIANT_CLUSTER, cluster_size=16)),
+    # the ring with small k: deeper rings that wrap many times per CTA
+    ("k2_T1500_stream", W.Workload("k2", T=1500, H=4096, k=2, E=16), dict(variant=mfr.VARIANT_STREAM)),
+    ("k4_H8192_T700_stream", W.Workload("k4w", T=700, H=8192, k=4, E=16), dict(variant=mfr.VARIANT_STREAM)),
 ]
 
 
