@@ -53,7 +53,8 @@ def _planned(inp):
     return f32(rout), bf16_bits(out)
 
 
-@pytest.mark.parametrize("wl", [W.TINY_REF, W.PREFILL.with_(T=1000), W.wide(64), W.STRESS.with_(T=300)],
+@pytest.mark.parametrize("wl", [W.TINY_REF, W.PREFILL.with_(T=1000), W.wide(64), W.STRESS.with_(T=300),
+                                W.Workload("k2", T=2000, H=4096, k=2, E=16)],   # 8-stage ring, many wraps
                          ids=lambda w: f"{w.name}_T{w.T}")
 def test_noalloc_matches_the_oracle_twice(lib, wl):
     inp = W.make_inputs(wl, "cuda")
