@@ -144,6 +144,7 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
     l.fp4 = fp4 ? 1 : 0;
     l.expert_norm = expert_norm ? 1 : 0;
     l.sf_tiled = (fp4 && sf_layout == MFR_SF_TILED_128x4) ? 1 : 0;
+    l.all_slots = mfr::ring_all_slots(T, H, k, fused, fp4, expert_norm) ? 1 : 0;
     l.variant = pol.variant;
     l.early_trigger = pol.early_trigger;
     l.cluster = pol.cluster;
@@ -156,7 +157,8 @@ int make_plan(mfr_plan_t* plan, int64_t T, int64_t H, int k, int64_t R, const mf
         l.smem_bytes = mfr::stream_smem_bytes(k, stages, fused);
         // the attribute is per kernel, shared by every plan: always the device
         // maximum, so a plan with a deeper ring never loses its setting
-        if ((e = mfr::stream_prepare(static_cast<int>(H), fused, fp4, ring_budget, expert_norm, l.sf_tiled != 0)) !=
+        if ((e = mfr::stream_prepare(static_cast<int>(H), fused, fp4, ring_budget, expert_norm, l.sf_tiled != 0,
+                                     l.all_slots != 0)) !=
             cudaSuccess) {
             cudaGetLastError();
             return fail_cuda(MFR_ERR_CUDA, "kernel attribute setup", e);

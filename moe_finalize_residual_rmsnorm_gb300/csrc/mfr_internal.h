@@ -49,6 +49,7 @@ struct Launch {
     int expert_norm;  // 1: RMSNorm per expert row before the weighted sum (mfr_expert_norm.cu)
     int prefetch_out; // 1: the small-call instantiation (residual loads after the rows; bf16 also prefetches its output lines)
     int sf_tiled;     // NVFP4: 1 = block scales in the 128 x 4 tiles block-scaled GEMMs read
+    int all_slots;    // ring kernel, residual + bf16, k = 8: the no-per-slot-test instantiation
 };
 
 // Sets the calling thread's moe_finalize_rmsnorm_last_error() text.
@@ -84,7 +85,8 @@ cudaError_t expert_norm_launch(const Params& p, const Launch& l, cudaStream_t s)
 int stream_threads();
 int stream_stage_bytes(int k, bool fused);
 int stream_smem_bytes(int k, int nstages, bool fused);
-cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en = false, bool sf_tiled = false);
+cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en = false, bool sf_tiled = false,
+                           bool all_slots = false);
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s);
 
 }  // namespace mfr

@@ -75,7 +75,8 @@ int setup_device(int dev, DeviceSetup* out) {
         // one attribute per kernel instantiation (by column tiles per token),
         // set to the device maximum exactly as the planned path sets it
         for (int h : {4096, 8192, 16384}) {
-            if (mfr::stream_prepare(h, true, false, budget) != cudaSuccess) {
+            if (mfr::stream_prepare(h, true, false, budget) != cudaSuccess ||
+                (h <= 8192 && mfr::stream_prepare(h, true, false, budget, false, false, true) != cudaSuccess)) {
                 cudaGetLastError();
                 return MFR_ERR_CUDA;
             }
@@ -158,6 +159,7 @@ extern "C" int moe_finalize_rmsnorm_run_noalloc(
     l.smem_bytes = mfr::stream_smem_bytes(k, stages, true);
     l.pdl = 1;
     l.fused = 1;
+    l.all_slots = mfr::ring_all_slots(T, H, k, true, false, false) ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* status = ds.status + slot;

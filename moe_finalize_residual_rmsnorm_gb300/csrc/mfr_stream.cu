@@ -68,8 +68,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // MAXTILES: upper bound on ceil(H / CB) for this instantiation;
 // FUSED: residual + RMSNorm (true) or plain finalize (false); EN: per-expert
 // RMSNorm (with FUSED = false); SFT (with FP4): block scales in the tiled
-// layout of block-scaled GEMMs instead of row-major.
-template <int MAXTILES, bool FUSED, bool FP4, bool EN, bool SFT = false>
+// layout of block-scaled GEMMs instead of row-major; AS (residual + bf16,
+// k = 8): tiles whose eight slots are all valid skip the per-slot tests
+// (ring_all_slots in mfr_policy.h says where this is taken).
+template <int MAXTILES, bool FUSED, bool FP4, bool EN, bool SFT = false, bool AS = false>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 stream_kernel(const Params p, const int nstages, const int stage_bytes)
 {
@@ -435,14 +437,33 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
 #pragma unroll
             for (int q = 0; q < kColsPT; ++q) acc[q] = 0.f;
             if (mine) {
+                // AS: k = 8 and every slot valid (a uniform test per tile): the
+                // eight slots' loads first, then the FMAs, with no per-slot
+                // tests (the NVFP4 form was 1-2 % slower with it)
+                if (AS && k == 8 && mask == 0xFFu) {
+                    uint2 v[8];
+                    float wv[8];
 #pragma unroll
-                for (int j = 0; j < kMaxK; ++j) {
-                    if (j < k && (mask & (1u << j))) {
-                        const float wj = hd->w[j];
-                        const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
-                        const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+                    for (int j = 0; j < 8; ++j) {
+                        v[j] = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
+                        wv[j] = hd->w[j];
+                    }
 #pragma unroll
-                        for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(wj, e[q], acc[q]);
+                    for (int j = 0; j < 8; ++j) {
+                        const float e[4] = {bf16_lo(v[j].x), bf16_hi(v[j].x), bf16_lo(v[j].y), bf16_hi(v[j].y)};
+#pragma unroll
+                        for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(wv[j], e[q], acc[q]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kMaxK; ++j) {
+                        if (j < k && (mask & (1u << j))) {
+                            const float wj = hd->w[j];
+                            const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
+                            const float e[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+#pragma unroll
+                            for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(wj, e[q], acc[q]);
+                        }
                     }
                 }
                 const float4 r = *reinterpret_cast<const float4*>(st + res_off + tid * 16);
@@ -509,15 +530,19 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
 using StreamKernel = void (*)(const Params, const int, const int);
 
 template <int MAXTILES>
-StreamKernel pick(bool fused, bool fp4, bool sft) {
+StreamKernel pick(bool fused, bool fp4, bool sft, bool as) {
     if (fp4) {
         if (!fused) return nullptr;
         return sft ? stream_kernel<MAXTILES, true, true, false, true> : stream_kernel<MAXTILES, true, true, false>;
     }
+    if constexpr (MAXTILES <= 4) {
+        if (fused && as) return stream_kernel<MAXTILES, true, false, false, false, true>;
+    }
+    if (as) return nullptr;   // not taken above 8192 columns
     return fused ? stream_kernel<MAXTILES, true, false, false> : stream_kernel<MAXTILES, false, false, false>;
 }
 
-StreamKernel stream_kernel_for(int H, bool fused, bool fp4, bool en, bool sft = false) {
+StreamKernel stream_kernel_for(int H, bool fused, bool fp4, bool en, bool sft = false, bool as = false) {
     const int tiles = (H + kStreamCB - 1) / kStreamCB;
     if (en) {
         if (fused || fp4) return nullptr;
@@ -525,9 +550,9 @@ StreamKernel stream_kernel_for(int H, bool fused, bool fp4, bool en, bool sft = 
         if (tiles <= 4) return stream_kernel<4, false, false, true>;
         return nullptr;
     }
-    if (tiles <= 2) return pick<2>(fused, fp4, sft);
-    if (tiles <= 4) return pick<4>(fused, fp4, sft);
-    if (tiles <= 8) return pick<8>(fused, fp4, sft);
+    if (tiles <= 2) return pick<2>(fused, fp4, sft, as);
+    if (tiles <= 4) return pick<4>(fused, fp4, sft, as);
+    if (tiles <= 8) return pick<8>(fused, fp4, sft, as);
     return nullptr;
 }
 
@@ -543,14 +568,15 @@ int stream_smem_bytes(int k, int nstages, bool fused) {
     return ((2 * nstages * 8 + 127) / 128) * 128 + nstages * stream_stage_bytes(k, fused);
 }
 
-cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en, bool sf_tiled) {
-    StreamKernel kf = stream_kernel_for(H, fused, fp4, en, sf_tiled);
+cudaError_t stream_prepare(int H, bool fused, bool fp4, int smem_bytes, bool en, bool sf_tiled, bool all_slots) {
+    StreamKernel kf = stream_kernel_for(H, fused, fp4, en, sf_tiled, all_slots);
     if (!kf) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
 cudaError_t stream_launch(const Params& p, const Launch& l, cudaStream_t s) {
-    StreamKernel kf = stream_kernel_for(p.H, l.fused != 0, l.fp4 != 0, l.expert_norm != 0, l.sf_tiled != 0);
+    StreamKernel kf = stream_kernel_for(p.H, l.fused != 0, l.fp4 != 0, l.expert_norm != 0, l.sf_tiled != 0,
+                                        l.all_slots != 0);
     if (!kf) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(l.grid_x), 1, 1);

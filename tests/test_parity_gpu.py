@@ -163,13 +163,15 @@ def test_stream_token_counts_around_the_sm_count(T, H):
 
 
 @pytest.mark.parametrize("k,H", [(1, 4096), (2, 4096), (4, 4096), (16, 4096), (4, 8192), (3, 1032),
-                                 (8, 16384), (2, 12288)])
+                                 (8, 16384), (2, 12288), (8, 4096), (8, 8192)])
 def test_stream_ring_wraps_at_every_depth(k, H):
     """Many tokens per CTA (T = 2000, or 700 at H > 8192, over at most 152
     CTAs) with every ring depth the plan gives, from 3 stages (k = 16) to 8
     (k <= 2): the ring wraps many times and the stage barriers' phases
     alternate (at H = 12288 and 16384 a token spans 6 and 8 tiles); every
-    token against the oracle, an out-of-range row included."""
+    token against the oracle, an out-of-range row included (with k = 8 at
+    H <= 8192 it sends that token's tiles through the general slot loop of
+    the all-slots instantiation)."""
     T = 2000 if H <= 8192 else 700
     inp = inputs_for(T, H, k, R=T * k + 5, seed=31 + k + H)
     inp["permuted_row_of"][T // 2, k - 1] = T * k + 5          # == R: invalid

@@ -34,6 +34,9 @@ extern "C" int policy_choose(long long T, long long H, int k, int fused, int fp4
     return rc;
 }
 extern "C" int policy_stream_grid(long long T, int sms) { return mfr::stream_grid(T, sms); }
+extern "C" int policy_all_slots(long long T, long long H, int k, int fused, int fp4, int en) {
+    return mfr::ring_all_slots(T, H, k, fused != 0, fp4 != 0, en != 0) ? 1 : 0;
+}
 '''
 
 
@@ -51,6 +54,8 @@ def lib(tmp_path_factory):
         [ctypes.POINTER(ctypes.c_int), ctypes.c_char_p, ctypes.c_int]
     L.policy_stream_grid.restype = ctypes.c_int
     L.policy_stream_grid.argtypes = [ctypes.c_longlong, ctypes.c_int]
+    L.policy_all_slots.restype = ctypes.c_int
+    L.policy_all_slots.argtypes = [ctypes.c_longlong, ctypes.c_longlong] + [ctypes.c_int] * 4
     return L
 
 
@@ -233,3 +238,18 @@ def test_every_choice_fits_its_kernel(lib):
         if en and c > 1:
             assert k <= 8 and o["cpt"] <= 2
     assert checked > 5000
+
+
+def test_ring_all_slots_instantiation(lib):
+    """The ring kernel's residual + bf16 form takes the no-per-slot-test
+    instantiation for k = 8 up to 2^24 elements at H <= 8192; never for
+    other k, other outputs, wider rows or larger calls."""
+    a = lambda T, H, k=8, fused=1, fp4=0, en=0: lib.policy_all_slots(T, H, k, fused, fp4, en)
+    assert a(1, 4096) == 1 and a(4096, 4096) == 1 and a(4097, 4096) == 0 and a(16384, 4096) == 0
+    assert a(2048, 8192) == 1 and a(2049, 8192) == 0 and a(32768, 8192) == 0
+    assert a(2730, 6144) == 1 and a(2731, 6144) == 0
+    assert a(16000, 1032) == 1
+    assert a(100, 8200) == 0 and a(100, 16384) == 0
+    for k in (1, 4, 7, 9, 16):
+        assert a(1000, 4096, k=k) == 0
+    assert a(1000, 4096, fp4=1) == 0 and a(1000, 4096, fused=0) == 0 and a(1000, 4096, fused=0, en=1) == 0
