@@ -45,19 +45,27 @@ constexpr int64_t kEarlyTriggerMaxElems = int64_t(1) << 19;
 // 1.81 -> 1.84 us without the prefetch taken).
 constexpr int64_t kPrefetchOutMaxElems = int64_t(1) << 15;
 
-// The ring kernel's residual + bf16 form with k = 8 has an instantiation
-// whose consumers, when all eight slots of a tile are valid, load the eight
-// row segments first and then run the FMAs with no per-slot tests.
-// Measured on GB300 against the general slot loop (same box, two rounds):
-// H = 4096, T = 512 / 1024 / 2048 / 4096 2.9 / 3.5 / 2.6 / 0.9 % faster;
-// H = 8192, T = 256 / 512 / 1024 / 2048 6.3 / 2.6 / 1.7 / 1.4 % faster;
-// prefill (T = 16384, H = 4096) within 0.3 % either way; at H = 8192,
-// T = 4096 / 8192 / 32768 0.7 / 1.8 / 1.5 % slower.  So it is taken up to
-// 2^24 elements at H <= 8192, and the larger calls keep the loop.
+// The ring kernel's residual + bf16 and plain finalize forms with k = 8
+// have an instantiation whose consumers, when all eight slots of a tile are
+// valid, load the eight row segments first and then run the FMAs with no
+// per-slot tests.  Measured on GB300 against the general slot loop (same
+// box, two rounds, outputs hashed equal):
+//  residual + bf16: H = 4096, T = 512 / 1024 / 2048 / 4096 2.9 / 3.5 / 2.6 /
+//    0.9 % faster; H = 8192, T = 256 / 512 / 1024 / 2048 6.3 / 2.6 / 1.7 /
+//    1.4 % faster; prefill (T = 16384, H = 4096) within 0.3 % either way;
+//    H = 8192, T = 4096 / 8192 / 32768 0.7 / 1.8 / 1.5 % slower;
+//  plain finalize: H = 4096, T = 1024 / 4096 / 16384 11 / 4.5 / 1.0 %
+//    faster; H = 8192, T = 512 17 % faster, T = 2048 / 4096 / 8192 0.5 /
+//    1.9 / 3.8 % slower.
+// So: residual + bf16 up to 2^24 elements at H <= 8192; plain finalize at
+// every size up to H = 4096 and up to 2^22 elements at H = 8192.  (The
+// per-expert RMSNorm form has the same path in its only instantiation.)
 constexpr int64_t kRingAllSlotsMaxElems = int64_t(1) << 24;
+constexpr int64_t kPlainAllSlotsMaxElems = int64_t(1) << 22;
 inline bool ring_all_slots(int64_t T, int64_t H, int k, bool fused, bool fp4, bool expert_norm) {
-    return fused && !fp4 && !expert_norm && k == 8 && H <= 4 * kStreamTileCols &&
-           T * H <= kRingAllSlotsMaxElems;
+    if (fp4 || expert_norm || k != 8 || H > 4 * kStreamTileCols) return false;
+    if (fused) return T * H <= kRingAllSlotsMaxElems;
+    return H <= 2 * kStreamTileCols || T * H <= kPlainAllSlotsMaxElems;
 }
 
 inline int round_up(int v, int m) { return (v + m - 1) / m * m; }

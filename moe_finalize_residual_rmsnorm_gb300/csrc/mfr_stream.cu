@@ -68,9 +68,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // MAXTILES: upper bound on ceil(H / CB) for this instantiation;
 // FUSED: residual + RMSNorm (true) or plain finalize (false); EN: per-expert
 // RMSNorm (with FUSED = false); SFT (with FP4): block scales in the tiled
-// layout of block-scaled GEMMs instead of row-major; AS (residual + bf16,
-// k = 8): tiles whose eight slots are all valid skip the per-slot tests
-// (ring_all_slots in mfr_policy.h says where this is taken).
+// layout of block-scaled GEMMs instead of row-major; AS (residual + bf16 or
+// plain finalize, k = 8): tiles whose eight slots are all valid skip the
+// per-slot tests (ring_all_slots in mfr_policy.h says where this is taken;
+// the per-expert RMSNorm form always has that path).
 template <int MAXTILES, bool FUSED, bool FP4, bool EN, bool SFT = false, bool AS = false>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 stream_kernel(const Params p, const int nstages, const int stage_bytes)
@@ -285,13 +286,29 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 const bool mine = tid * kColsPT < min(kStreamCB, H - c0);
                 const bool in_regs = b < kRegTiles;       // a constant: the loop is unrolled
                 const int rb = in_regs ? b : 0;
+                if (k == 8 && mask == 0xFFu && mine) {
+                    // all eight slots valid: the eight loads first, then the
+                    // sums of squares, with no per-slot tests (measured on
+                    // GB300: 0.3-4.0 % faster at every size from T = 512 to
+                    // 16384, H = 4096 and 8192; prefill 181.7 -> 174.5 us)
+                    uint2 vv[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (in_regs) rv[rb][j] = make_uint2(0, 0);
-                    if (j < k && (mask & (1u << j)) && mine) {
-                        const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
-                        if (in_regs) rv[rb][j] = v;
-                        ss[j] = sumsq_bf16x4(v, ss[j]);   // bf16 operands straight into the FMA
+                    for (int j = 0; j < 8; ++j)
+                        vv[j] = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (in_regs) rv[rb][j] = vv[j];
+                        ss[j] = sumsq_bf16x4(vv[j], ss[j]);   // bf16 operands straight into the FMA
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (in_regs) rv[rb][j] = make_uint2(0, 0);
+                        if (j < k && (mask & (1u << j)) && mine) {
+                            const uint2 v = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
+                            if (in_regs) rv[rb][j] = v;
+                            ss[j] = sumsq_bf16x4(v, ss[j]);
+                        }
                     }
                 }
                 if (in_regs) {
@@ -389,7 +406,22 @@ stream_kernel(const Params p, const int nstages, const int stage_bytes)
                 float acc[kColsPT];
 #pragma unroll
                 for (int q = 0; q < kColsPT; ++q) acc[q] = 0.f;
-                if (mine) {
+                if (mine && AS && k == 8 && mask == 0xFFu) {
+                    // AS: all eight slots valid: loads first, FMAs without per-slot tests
+                    uint2 v[8];
+                    float wv[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        v[j] = *reinterpret_cast<const uint2*>(st + kHeaderBytes + j * row_bytes + tid * 8);
+                        wv[j] = hd->w[j];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float e[4] = {bf16_lo(v[j].x), bf16_hi(v[j].x), bf16_lo(v[j].y), bf16_hi(v[j].y)};
+#pragma unroll
+                        for (int q = 0; q < kColsPT; ++q) acc[q] = __fmaf_rn(wv[j], e[q], acc[q]);
+                    }
+                } else if (mine) {
 #pragma unroll
                     for (int j = 0; j < kMaxK; ++j) {
                         if (j < k && (mask & (1u << j))) {
@@ -536,7 +568,8 @@ StreamKernel pick(bool fused, bool fp4, bool sft, bool as) {
         return sft ? stream_kernel<MAXTILES, true, true, false, true> : stream_kernel<MAXTILES, true, true, false>;
     }
     if constexpr (MAXTILES <= 4) {
-        if (fused && as) return stream_kernel<MAXTILES, true, false, false, false, true>;
+        if (as) return fused ? stream_kernel<MAXTILES, true, false, false, false, true>
+                             : stream_kernel<MAXTILES, false, false, false, false, true>;
     }
     if (as) return nullptr;   // not taken above 8192 columns
     return fused ? stream_kernel<MAXTILES, true, false, false> : stream_kernel<MAXTILES, false, false, false>;

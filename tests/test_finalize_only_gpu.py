@@ -55,10 +55,13 @@ def test_finalize_only_matches_oracle(kw, T, H, k):
     assert plan.get_status() == 0
 
 
-@pytest.mark.parametrize("T,H,k", [(2000, 4096, 2), (1500, 8192, 4), (1800, 4096, 16)])
+@pytest.mark.parametrize("T,H,k", [(2000, 4096, 2), (1500, 8192, 4), (1800, 4096, 16), (2000, 4096, 8),
+                                   (512, 8192, 8), (2048, 8192, 8)])
 def test_finalize_only_ring_wraps(T, H, k):
     """The ring form with ring depths from 3 stages (k = 16) to 8 (k = 2) and
-    many tokens per CTA: every token bitwise equal to the oracle."""
+    many tokens per CTA, with k = 8 in both the all-slots instantiation
+    (H = 4096; H = 8192 up to 2^22 elements) and the general one: every
+    token bitwise equal to the oracle."""
     wl = W.Workload(f"fin_ring_T{T}_H{H}_k{k}", T=T, H=H, k=k, E=max(16, 2 * k), seed=T + H + k, extra_rows=2)
     inp = W.make_inputs(wl, "cuda")
     want, bad = oracle_finalize_only(inp)
@@ -67,6 +70,21 @@ def test_finalize_only_ring_wraps(T, H, k):
     assert np.array_equal(got, want)
     assert plan.get_status() == 0
     assert plan.info()["variant"] == mfr.VARIANT_STREAM
+
+
+@pytest.mark.parametrize("T,H", [(1500, 4096), (400, 8192)])
+def test_finalize_only_ring_bad_slot_in_the_all_slots_form(T, H):
+    """k = 8 in the ring's all-slots instantiation: a token with an
+    out-of-range slot takes the general slot loop, adds nothing for that
+    slot and raises the status bit; every token bitwise equal to the oracle."""
+    wl = W.Workload(f"fin_bad_T{T}_H{H}", T=T, H=H, k=8, E=16, seed=T + H, extra_rows=2)
+    inp = W.make_inputs(wl, "cuda")
+    inp["permuted_row_of"][T // 3, 3] = wl.R          # == R: invalid
+    want, bad = oracle_finalize_only(inp)
+    assert bad == 1
+    got, plan = run_finalize(inp, variant=mfr.VARIANT_STREAM)
+    assert np.array_equal(got, want)
+    assert plan.get_status() & mfr.STATUS_BAD_INDEX
 
 
 @pytest.mark.parametrize("T,H", [(1, 4096), (4, 4096), (2, 8192), (33, 8192)])

@@ -241,15 +241,20 @@ def test_every_choice_fits_its_kernel(lib):
 
 
 def test_ring_all_slots_instantiation(lib):
-    """The ring kernel's residual + bf16 form takes the no-per-slot-test
-    instantiation for k = 8 up to 2^24 elements at H <= 8192; never for
-    other k, other outputs, wider rows or larger calls."""
+    """The ring kernel takes the no-per-slot-test instantiation for k = 8:
+    the residual + bf16 form up to 2^24 elements at H <= 8192, the plain
+    finalize at every size up to H = 4096 and up to 2^22 elements at
+    H = 8192; never for other k, the NVFP4 output or wider rows."""
     a = lambda T, H, k=8, fused=1, fp4=0, en=0: lib.policy_all_slots(T, H, k, fused, fp4, en)
     assert a(1, 4096) == 1 and a(4096, 4096) == 1 and a(4097, 4096) == 0 and a(16384, 4096) == 0
     assert a(2048, 8192) == 1 and a(2049, 8192) == 0 and a(32768, 8192) == 0
     assert a(2730, 6144) == 1 and a(2731, 6144) == 0
     assert a(16000, 1032) == 1
     assert a(100, 8200) == 0 and a(100, 16384) == 0
+    fin = lambda T, H, k=8: a(T, H, k=k, fused=0)
+    assert fin(16384, 4096) == 1 and fin(1 << 20, 2048) == 1
+    assert fin(512, 8192) == 1 and fin(513, 8192) == 0 and fin(8192, 8192) == 0
+    assert fin(100, 8200) == 0 and fin(100, 16384) == 0
     for k in (1, 4, 7, 9, 16):
-        assert a(1000, 4096, k=k) == 0
-    assert a(1000, 4096, fp4=1) == 0 and a(1000, 4096, fused=0) == 0 and a(1000, 4096, fused=0, en=1) == 0
+        assert a(1000, 4096, k=k) == 0 and fin(1000, 4096, k=k) == 0
+    assert a(1000, 4096, fp4=1) == 0 and a(1000, 4096, fused=0, en=1) == 0
