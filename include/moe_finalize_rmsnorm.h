@@ -310,9 +310,9 @@ void moe_finalize_rmsnorm_destroy(mfr_plan_t plan);
  * with r_j = permuted_row_of[t, j], FP32 fused multiply-adds in slot order
  * j = 0..k-1, the shared gamma, and no residual.  Variants: a cluster of
  * CTAs per token that split H (MFR_VARIANT_CLUSTER, k <= 8; chosen for
- * T*H <= 2^19), one CTA per token (MFR_VARIANT_ROWS), and for
- * T*H >= 1.5*2^20 with k <= 8 and H <= 8192 the persistent ring kernel
- * (MFR_VARIANT_STREAM).  Forcing CLUSTER with k > 8, or STREAM outside its
+ * T*H <= 2^19), one CTA per token (MFR_VARIANT_ROWS), and above one wave
+ * of those (T*H > 8192 x the SM count) with k <= 8 and H <= 8192 the
+ * persistent ring kernel (MFR_VARIANT_STREAM).  Forcing CLUSTER with k > 8, or STREAM outside its
  * limits, is MFR_ERR_UNSUPPORTED_SHAPE.
  *
  * moe_finalize_expert_rmsnorm_plan: as moe_finalize_rmsnorm_plan (same

@@ -21,13 +21,23 @@ constexpr int kMaxStages = 8;           // ring kernel: deepest ring
 // Variant choice by the number of elements T*H of a call (measured on GB300
 // with cold inputs, CUDA graph): up to 2^19 a cluster of CTAs per token is
 // fastest (few tokens, latency bound; decode_cluster, finalize_split and
-// en_cluster pick its size per plan kind); below
-// 1.5*2^20 one CTA per token; from there the persistent ring kernel (its
-// per-SM pipeline needs a few tokens per SM: at 1.5*2^20 it is 8 % faster at
-// H = 4096 and 3 % slower at H = 8192, at 2^21 faster at both, at 3*2^20 by
-// 9-15 %).  Small grids signal their dependents at entry.
+// en_cluster pick its size per plan kind); above that one CTA per token
+// while its grid is one wave, 8192 elements per SM (304 tokens at H = 4096,
+// two CTAs per SM; 152 at H = 8192), and the persistent ring kernel from
+// there.  Measured with the ring's all-slots form, forced variants: at the
+// wave boundary one CTA per token is 2-19 % faster for every output; one
+// wave above it (T = 320 / 352 at H = 4096, 160 / 176 at H = 8192) the ring
+// is faster for the residual + bf16 (0.4-6.5 %), plain finalize (2-7.5 %)
+// and per-expert RMSNorm (6-16 %) outputs, but 4-6.5 % slower for NVFP4,
+// which keeps one CTA per token below 1.5*2^20 (there the ring was 8 %
+// faster at H = 4096 and 3 % slower at H = 8192, at 2^21 faster at both).
+// Small grids signal their dependents at entry.
 constexpr int64_t kClusterMaxElems = int64_t(1) << 19;
-constexpr int64_t kRowsMaxElems = int64_t(3) << 19;
+constexpr int64_t kRowsMaxElems = int64_t(3) << 19;      // NVFP4: ring from here
+constexpr int64_t kRowsElemsPerSm = 8192;                // other outputs: one wave of rows CTAs
+inline bool rows_beats_ring(int64_t elems, bool fp4, int sms) {
+    return fp4 ? elems < kRowsMaxElems : elems <= kRowsElemsPerSm * sms;
+}
 constexpr int64_t kEarlyTriggerMaxElems = int64_t(1) << 19;
 // Calls this small leave HBM idle, so the fused bf16 kernel also asks L2 for
 // its output lines before the dependency wait, so the stores at the end hit,
@@ -204,7 +214,8 @@ inline int choose_launch(const PolicyIn& in, PolicyOut* out, char* err, size_t e
                 if (csize == 0) csize = en_cluster(chunks, elems);
                 variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
             } else {
-                variant = (ring_ok && elems >= kRowsMaxElems) ? MFR_VARIANT_STREAM : MFR_VARIANT_ROWS;
+                variant = (ring_ok && !rows_beats_ring(elems, false, in.sms)) ? MFR_VARIANT_STREAM
+                                                                                 : MFR_VARIANT_ROWS;
             }
         }
     }
@@ -220,7 +231,7 @@ inline int choose_launch(const PolicyIn& in, PolicyOut* out, char* err, size_t e
                     csize = split_for_threads(chunks, 64);
             }
             variant = csize > 1 ? MFR_VARIANT_CLUSTER : MFR_VARIANT_ROWS;
-        } else if (elems < kRowsMaxElems || in.stages < 2) {
+        } else if (rows_beats_ring(elems, in.fp4, in.sms) || in.stages < 2) {
             variant = MFR_VARIANT_ROWS;
         } else {
             variant = MFR_VARIANT_STREAM;

@@ -202,13 +202,14 @@ def test_rows_kernel_both_slot_forms(T):
 @pytest.mark.parametrize("T,H,variant,cluster", [
     (1, 4096, mfr.VARIANT_CLUSTER, 4), (4, 4096, mfr.VARIANT_CLUSTER, 4), (8, 4096, mfr.VARIANT_CLUSTER, 16),
     (32, 4096, mfr.VARIANT_CLUSTER, 16), (64, 4096, mfr.VARIANT_CLUSTER, 8), (128, 4096, mfr.VARIANT_CLUSTER, 2),
-    (129, 4096, mfr.VARIANT_ROWS, 1), (383, 4096, mfr.VARIANT_ROWS, 1), (384, 4096, mfr.VARIANT_STREAM, 1),
+    (129, 4096, mfr.VARIANT_ROWS, 1), (304, 4096, mfr.VARIANT_ROWS, 1), (305, 4096, mfr.VARIANT_STREAM, 1),
     (1, 8192, mfr.VARIANT_CLUSTER, 8), (8, 8192, mfr.VARIANT_CLUSTER, 16), (64, 8192, mfr.VARIANT_CLUSTER, 4),
-    (65, 8192, mfr.VARIANT_ROWS, 1), (192, 8192, mfr.VARIANT_STREAM, 1), (2, 1024, mfr.VARIANT_ROWS, 1)])
+    (65, 8192, mfr.VARIANT_ROWS, 1), (152, 8192, mfr.VARIANT_ROWS, 1), (153, 8192, mfr.VARIANT_STREAM, 1),
+    (2, 1024, mfr.VARIANT_ROWS, 1)])
 def test_automatic_plan_choices(T, H, variant, cluster):
     """The variant and cluster size the plan picks by T*H (measured
-    thresholds: clusters up to 2^19 elements, one CTA per token below
-    1.5*2^20, the ring from there)."""
+    thresholds: clusters up to 2^19 elements, one CTA per token up to one
+    wave (8192 elements per SM), the ring from there)."""
     info = mfr.Plan(T, H, 8).info()
     assert (info["variant"], info["cluster"]) == (variant, cluster)
 

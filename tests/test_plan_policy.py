@@ -72,11 +72,13 @@ AUTO_TABLE = [
     (1, 4096, mfr.VARIANT_CLUSTER, 4), (4, 4096, mfr.VARIANT_CLUSTER, 4), (5, 4096, mfr.VARIANT_CLUSTER, 16),
     (8, 4096, mfr.VARIANT_CLUSTER, 16), (32, 4096, mfr.VARIANT_CLUSTER, 16), (33, 4096, mfr.VARIANT_CLUSTER, 8),
     (64, 4096, mfr.VARIANT_CLUSTER, 8), (65, 4096, mfr.VARIANT_CLUSTER, 2), (128, 4096, mfr.VARIANT_CLUSTER, 2),
-    (129, 4096, mfr.VARIANT_ROWS, 1), (383, 4096, mfr.VARIANT_ROWS, 1), (384, 4096, mfr.VARIANT_STREAM, 1),
+    (129, 4096, mfr.VARIANT_ROWS, 1), (304, 4096, mfr.VARIANT_ROWS, 1), (305, 4096, mfr.VARIANT_STREAM, 1),
+    (384, 4096, mfr.VARIANT_STREAM, 1),
     (16384, 4096, mfr.VARIANT_STREAM, 1),
     (1, 8192, mfr.VARIANT_CLUSTER, 8), (2, 8192, mfr.VARIANT_CLUSTER, 8), (3, 8192, mfr.VARIANT_CLUSTER, 16),
     (16, 8192, mfr.VARIANT_CLUSTER, 16), (32, 8192, mfr.VARIANT_CLUSTER, 8), (64, 8192, mfr.VARIANT_CLUSTER, 4),
-    (65, 8192, mfr.VARIANT_ROWS, 1), (191, 8192, mfr.VARIANT_ROWS, 1), (192, 8192, mfr.VARIANT_STREAM, 1),
+    (65, 8192, mfr.VARIANT_ROWS, 1), (152, 8192, mfr.VARIANT_ROWS, 1), (153, 8192, mfr.VARIANT_STREAM, 1),
+    (192, 8192, mfr.VARIANT_STREAM, 1),
     (2, 1024, mfr.VARIANT_ROWS, 1), (32, 1024, mfr.VARIANT_CLUSTER, 4), (1, 16384, mfr.VARIANT_CLUSTER, 16),
 ]
 
@@ -258,3 +260,19 @@ def test_ring_all_slots_instantiation(lib):
     for k in (1, 4, 7, 9, 16):
         assert a(1000, 4096, k=k) == 0 and fin(1000, 4096, k=k) == 0
     assert a(1000, 4096, fp4=1) == 0 and a(1000, 4096, fused=0, en=1) == 0
+
+
+def test_rows_to_ring_at_one_wave(lib):
+    """One CTA per token while its grid is one wave (8192 elements per SM:
+    304 tokens at H = 4096, 152 at H = 8192), the ring above, for the
+    residual + bf16, plain finalize and per-expert RMSNorm outputs; the
+    NVFP4 output keeps one CTA per token below 1.5 * 2^20 elements."""
+    for kw in (dict(), dict(fused=False), dict(fused=False, en=True)):
+        for T, H, want in ((304, 4096, mfr.VARIANT_ROWS), (305, 4096, mfr.VARIANT_STREAM),
+                           (152, 8192, mfr.VARIANT_ROWS), (153, 8192, mfr.VARIANT_STREAM)):
+            rc, o, _ = choose(lib, T, H, **kw)
+            assert rc == 0 and o["variant"] == want, (kw, T, H)
+    for T, H, want in ((305, 4096, mfr.VARIANT_ROWS), (383, 4096, mfr.VARIANT_ROWS), (384, 4096, mfr.VARIANT_STREAM),
+                       (191, 8192, mfr.VARIANT_ROWS), (192, 8192, mfr.VARIANT_STREAM)):
+        rc, o, _ = choose(lib, T, H, fp4=True)
+        assert rc == 0 and o["variant"] == want, (T, H)
