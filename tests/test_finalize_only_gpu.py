@@ -56,12 +56,12 @@ def test_finalize_only_matches_oracle(kw, T, H, k):
 
 
 @pytest.mark.parametrize("T,H,k", [(2000, 4096, 2), (1500, 8192, 4), (1800, 4096, 16), (2000, 4096, 8),
-                                   (512, 8192, 8), (2048, 8192, 8)])
+                                   (512, 8192, 8), (2048, 8192, 8), (300, 24, 8), (400, 136, 8), (300, 2056, 8)])
 def test_finalize_only_ring_wraps(T, H, k):
     """The ring form with ring depths from 3 stages (k = 16) to 8 (k = 2) and
     many tokens per CTA, with k = 8 in both the all-slots instantiation
-    (H = 4096; H = 8192 up to 2^22 elements) and the general one: every
-    token bitwise equal to the oracle."""
+    (H <= 4096, ragged widths included; H = 8192 up to 2^22 elements) and
+    the general one: every token bitwise equal to the oracle."""
     wl = W.Workload(f"fin_ring_T{T}_H{H}_k{k}", T=T, H=H, k=k, E=max(16, 2 * k), seed=T + H + k, extra_rows=2)
     inp = W.make_inputs(wl, "cuda")
     want, bad = oracle_finalize_only(inp)
